@@ -1,0 +1,423 @@
+"""Benchmark: one Ulysses attention layer step (fwd + bwd) on the GPU.
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+for every virtual rank and UPipe chunk, seq2head of Q/K/V, attention forward,
+head2seq of O; then seq2head of O/dO (plus Q/K/V again), attention backward,
+head2seq of dQ/dK/dV.  Default workload: the Qwen3-4B-shaped layer at S=65536
+(H_q=32, H_kv=8, D=128, P=4 virtual ranks, head_chunk=8, bf16 N(0,1) inputs).
+
+Prints one JSON line.  `value` is tokens/s of the whole step with inputs
+resident in HBM; `e2e` is the same through the public layer API with the
+inputs copied from pinned host memory and the outputs copied back inside the
+timed region.  `--impl reference` times the fp64 CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from long_context_sequence_seq_gb300 import inputs  # noqa: E402
+
+METRIC = "causal attn fwd+bwd tokens/s & TFLOPS at S=64K (% BF16 peak); re-layout GB/s"
+UNIT = "tokens/s"
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("bf16_tflops_sustained", p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def pairs_total(w, cu):
+    """Unmasked (i, j) pairs per head (host arithmetic on the mask only)."""
+    if cu is None:
+        return w.S * (w.S + 1) // 2 if w.causal else w.S * w.S
+    L = np.diff(np.asarray(cu, dtype=np.int64))
+    return int(np.sum(L * (L + 1) // 2)) if w.causal else int(np.sum(L * L))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class LayerStep:
+    """Device-resident buffers and the per-stage C-ABI call sequence of one step.
+
+    Attention calls are bracketed by CUDA events on the launching stream so
+    the dominant kernels' average durations come from the timed region itself.
+    """
+
+    def __init__(self, w, dev, cu_np):
+        from long_context_sequence_seq_gb300 import ulysses as U
+        self.U = U
+        self.w = w
+        q, k, v, do = inputs.make_seq_inputs(w, device=dev, small_on_host=False)
+        self.q, self.k, self.v, self.do = q, k, v, do
+        self.cu = None if cu_np is None else torch.from_numpy(cu_np).to(dev)
+        self.o = torch.empty_like(q)
+        self.lse = torch.empty((w.B, w.H_q, w.S), dtype=torch.float32, device=dev)
+        self.dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+        self.dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+        self.dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+        C, G = w.head_chunk, w.G
+        S, B, D = w.S, w.B, w.D
+        mk = lambda n, dt: torch.empty((B, n, S, D), dtype=dt, device=dev)  # noqa: E731
+        dt = q.dtype
+        self.qh, self.oh, self.doh = mk(C, dt), mk(C, dt), mk(C, dt)
+        self.kh, self.vh = mk(C // G, dt), mk(C // G, dt)
+        self.dqh = mk(C, torch.float32)
+        self.dkh, self.dvh = mk(C // G, torch.float32), mk(C // G, torch.float32)
+        self.lseh = torch.empty((B, C, S), dtype=torch.float32, device=dev)
+        wsb = U.attn_bwd_workspace_bytes(S, B, w.H_q, w.H_kv, D, w.P, C, 0,
+                                         U.BF16 if w.dtype == "bf16" else U.FP32)
+        self.ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
+        self.stages = w.P * (w.H_q // w.P // C)
+        self.events = []
+
+    def run(self, timed=False):
+        U, w = self.U, self.w
+        C, G = w.head_chunk, w.G
+        ev = []
+        for st in range(self.stages):
+            U.seq2head(self.q, w.P, C, st, out=self.qh)
+            U.seq2head(self.k, w.P, C // G, st, out=self.kh)
+            U.seq2head(self.v, w.P, C // G, st, out=self.vh)
+            e0 = torch.cuda.Event(enable_timing=True) if timed else None
+            e1 = torch.cuda.Event(enable_timing=True) if timed else None
+            if timed:
+                e0.record()
+            U.attn_fwd(self.qh, self.kh, self.vh, w.H_q, w.H_kv, w.P, C, st, self.cu, w.causal,
+                       out=self.oh, lse=self.lseh)
+            if timed:
+                e1.record()
+            U.head2seq(self.oh, self.o, w.P, C, st)
+            U.seq2head(self.do, w.P, C, st, out=self.doh)
+            e2 = torch.cuda.Event(enable_timing=True) if timed else None
+            e3 = torch.cuda.Event(enable_timing=True) if timed else None
+            if timed:
+                e2.record()
+            U.attn_bwd(self.qh, self.kh, self.vh, self.oh, self.doh, self.lseh, w.H_q, w.H_kv,
+                       w.P, C, st, self.cu, w.causal, workspace=self.ws, dq=self.dqh,
+                       dk=self.dkh, dv=self.dvh)
+            if timed:
+                e3.record()
+            U.head2seq(self.dqh, self.dq, w.P, C, st)
+            U.head2seq(self.dkh, self.dk, w.P, C // G, st)
+            U.head2seq(self.dvh, self.dv, w.P, C // G, st)
+            if timed:
+                ev.append((e0, e1, e2, e3))
+        if timed:
+            self.events.append(ev)
+
+
+def relayout_bytes_per_step(w):
+    elt = 2 if w.dtype == "bf16" else 4
+    n_q = w.B * w.S * w.H_q * w.D
+    n_kv = w.B * w.S * w.H_kv * w.D
+    fwd = 2 * (n_q + 2 * n_kv) * elt + 2 * n_q * elt          # Q,K,V in; O out
+    bwd = 2 * n_q * elt + 2 * (n_q + 2 * n_kv) * 4            # dO in; dQ,dK,dV out (fp32)
+    # the step re-uses the forward's head-layout Q/K/V/O for the backward
+    return fwd + bwd
+
+
+def measure_relayout(w, dev, reps=10):
+    """Isolated K1 timing on the Q tensor (inputs larger than L2)."""
+    from long_context_sequence_seq_gb300 import ulysses as U
+    x = torch.empty((w.B, w.S, w.H_q, w.D), dtype=torch.bfloat16 if w.dtype == "bf16" else torch.float32,
+                    device=dev)
+    x.view(torch.int16 if x.element_size() == 2 else torch.int32).random_(0, 1000)
+    out = torch.empty((w.B, w.H_q, w.S, w.D), dtype=x.dtype, device=dev)
+    for _ in range(3):
+        U.seq2head(x, w.P, None, None, out=out)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        U.seq2head(x, w.P, None, None, out=out)
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / 1e3)
+    byts = 2 * x.numel() * x.element_size()
+    del x, out
+    return byts / statistics.median(ts) / 1e9, byts
+
+
+def e2e_measure(w, dev, cu_np, steps, warmup):
+    """The public layer API with host buffers: H2D inputs, fwd+bwd, D2H outputs."""
+    from long_context_sequence_seq_gb300 import ulysses as U
+    dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    hq, hk, hv, hdo = (t.cpu().pin_memory() for t in inputs.make_seq_inputs(w, device=dev, small_on_host=False))
+    q, k, v, do = (torch.empty(t.shape, dtype=dt, device=dev) for t in (hq, hk, hv, hdo))
+    ws = U.layer_workspace(w.S, w.B, w.H_q, w.H_kv, w.D, w.P, w.head_chunk,
+                           U.BF16 if w.dtype == "bf16" else U.FP32, dev)
+    cu = None if cu_np is None else torch.from_numpy(cu_np).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H_q, w.S), dtype=torch.float32, device=dev)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+    ho = torch.empty(o.shape, dtype=dt).pin_memory()
+    hdq = torch.empty(dq.shape, dtype=torch.float32).pin_memory()
+    hdk = torch.empty(dk.shape, dtype=torch.float32).pin_memory()
+    hdv = torch.empty(dv.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv))
+
+    def step():
+        for d_, h_ in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+            d_.copy_(h_, non_blocking=True)
+        U.layer_fwd(q, k, v, w.P, w.head_chunk, cu, w.causal, workspace=ws, out=o, lse=lse)
+        U.layer_bwd(q, k, v, o, do, lse, w.P, w.head_chunk, cu, w.causal, workspace=ws,
+                    dq=dq, dk=dk, dv=dv)
+        for h_, d_ in ((ho, o), (hdq, dq), (hdk, dk), (hdv, dv)):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    U.check()
+    t = a.elapsed_time(b) / 1e3 / steps
+    return {"value": w.B * w.S / t, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": t * 1e3}
+
+
+def cpu_baseline(w, cu_np, budget_s=12.0):
+    """The fp64 oracle as it stands on the host cores, on a bounded sample:
+    forward + backward of one (q head, kv head) pair over a causal prefix of
+    the sequence.  Reported as the full-workload tokens/s it implies
+    (pairs per second of the oracle, scaled to all heads and pairs)."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    L = 2048
+    rng = np.random.Generator(np.random.PCG64(0))
+    while True:
+        q = rng.standard_normal((1, L, w.D))
+        k = rng.standard_normal((1, L, w.D))
+        v = rng.standard_normal((1, L, w.D))
+        do = rng.standard_normal((1, L, w.D))
+        t0 = time.perf_counter()
+        oracle.attn_fwd(q, k, v)
+        oracle.attn_bwd(q, k, v, do)
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 4 or L >= w.S:
+            break
+        L = min(w.S, L * 2)
+    pairs_s = (L * (L + 1) / 2) / dt
+    cu = cu_np
+    total = pairs_total(w, cu) * w.H_q * w.B
+    step_s = total / pairs_s
+    return {"value": w.B * w.S / step_s, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"fp64 oracle fwd+bwd of one q head over a {L}-token causal prefix "
+                      f"({dt:.2f} s), scaled by unmasked pairs to all {w.H_q} heads",
+            "sample_seconds": dt}
+
+
+def gpu_arm(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    from long_context_sequence_seq_gb300 import ulysses as U
+    U.lib()
+    w = inputs.WORKLOADS[args.workload]
+    cu_np = inputs.workload_cu_seqlens(w)
+    step = LayerStep(w, dev, cu_np)
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    U.check()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    n0 = U.launch_count()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(args.steps):
+        step.run(timed=True)
+    end.record()
+    torch.cuda.synchronize()
+    launches = U.launch_count() - n0
+    clk = clocks.stop()
+    U.check()
+    elapsed = start.elapsed_time(end) / 1e3
+    if world > 1:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+        dist.barrier()
+    t_step = elapsed / args.steps
+    fwd_t = [sum(e0.elapsed_time(e1) for e0, e1, _, _ in ev) / 1e3 for ev in step.events]
+    bwd_t = [sum(e2.elapsed_time(e3) for _, _, e2, e3 in ev) / 1e3 for ev in step.events]
+    n_launch_attn = step.stages
+    pairs = pairs_total(w, cu_np) * w.H_q * w.B
+    fl_fwd, fl_bwd = 4.0 * w.D * pairs, 10.0 * w.D * pairs
+    t_fwd, t_bwd = statistics.mean(fwd_t), statistics.mean(bwd_t)
+    hbm, bf16, bf16_sus, peak_src = load_peaks()
+    relay_gbs, _ = measure_relayout(w, dev)
+    del step
+    torch.cuda.empty_cache()
+    e2e = e2e_measure(w, dev, cu_np, max(1, args.steps // 2), max(1, args.warmup // 2))
+    # dominant kernel = attention backward (2.5x the forward's FLOPs)
+    bwd_per_launch_s = t_bwd / n_launch_attn
+    achieved = fl_bwd / n_launch_attn / bwd_per_launch_s / 1e12
+    res = {
+        "metric": METRIC, "value": world * w.B * w.S / t_step, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic N(0,1), seeded",
+        "config": {"workload": w.name, "S": w.S, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
+                   "D": w.D, "P": w.P, "head_chunk": w.head_chunk, "causal": w.causal,
+                   "packed": w.packed, "l2": "inputs larger than L2 (no flush needed)",
+                   "parallelism": f"{w.P} virtual ranks on one GPU" + (f", {world} replicas" if world > 1 else "")},
+        "tflops_fwd_bwd": (fl_fwd + fl_bwd) / (t_fwd + t_bwd) / 1e12,
+        "attn_fwd_ms": t_fwd * 1e3, "attn_bwd_ms": t_bwd * 1e3,
+        "attn_fwd_tflops": fl_fwd / t_fwd / 1e12, "attn_bwd_tflops": fl_bwd / t_bwd / 1e12,
+        "frac_fwd_bwd_of_bf16_peak": (fl_fwd + fl_bwd) / (t_fwd + t_bwd) / 1e12 / bf16,
+        "relayout_gbs": relay_gbs, "relayout_frac_hbm": relay_gbs / hbm,
+        "relayout_bytes_per_step": relayout_bytes_per_step(w),
+        "roofline": {"kernel": "attn_bwd", "bound": "tensor", "achieved": achieved,
+                     "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16, "traffic": None,
+                     "peak_source": f"{peak_src} bf16 dense (burst)"},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "e2e": e2e,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, cu_np)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def reference_arm(args):
+    """The fp64 CPU oracle on the host cores (rank 0 only), one bounded sample
+    per step, reported as the full-workload tokens/s the sample implies."""
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    w = inputs.WORKLOADS[args.workload]
+    cu_np = inputs.workload_cu_seqlens(w)
+    for _ in range(args.warmup):
+        cpu_baseline(w, cu_np, budget_s=2.0)
+    vals, secs = [], []
+    for _ in range(args.steps):
+        r = cpu_baseline(w, cu_np, budget_s=2.0)
+        vals.append(r["value"])
+        secs.append(r["sample_seconds"])
+    v = statistics.median(vals)
+    res = {"metric": METRIC, "value": v, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": statistics.median(secs) * 1e3,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic N(0,1), seeded", "impl": "reference",
+           "config": {"workload": w.name, "S": w.S, "H_q": w.H_q, "H_kv": w.H_kv, "D": w.D,
+                      "P": w.P, "head_chunk": w.head_chunk},
+           "cpu_baseline": {"value": v, "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                            "sample": r["sample"]},
+           "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(res), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="qwen3_4b_64k", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

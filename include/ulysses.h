@@ -1,0 +1,177 @@
+/*
+ * ulysses.h — C ABI of the single-GPU Ulysses sequence-parallel attention path.
+ *
+ * What the calls compute (page "Ulysses Sequence Parallelism for million-token
+ * context training", section "How Ulysses sequence parallelism works"):
+ *   step 1  every rank holds a contiguous chunk of S/P tokens with all heads
+ *           (the "sequence layout" below);
+ *   step 3  an all-to-all leaves every rank with all S positions for its subset
+ *           of heads  -> ulysses_seq2head;
+ *   step 4  local dense attention over the whole sequence for those heads
+ *           -> ulysses_attn_fwd / ulysses_attn_bwd;
+ *   step 5  a second all-to-all restores the sequence-sharded form
+ *           -> ulysses_head2seq.
+ * The P ranks are P partitions of one device buffer, so each all-to-all is an
+ * on-device permutation.  UPipe head chunking (page "Ulysses Sequence
+ * Parallelism" commentary, section on contexts beyond a million tokens:
+ * process only some heads at a time) is the `head_chunk` / `stage` pair.
+ *
+ * Layouts (row-major, element size 2 bytes for BF16, 4 for FP32):
+ *   sequence layout  X_seq [B][S][H][D]      rank r owns tokens [r*S/P, (r+1)*S/P)
+ *   head layout      X_head[B][n][S][D]      n = heads of the selected stage
+ *   permutation      X_head[b][h'][t][d] = X_seq[b][t][h0 + h'][d]
+ *   where rank r owns heads [r*H/P, (r+1)*H/P) and stage s = r*(hq/C) + c
+ *   starts at h0 = r*hq + c*C (hq = H/P, C = head_chunk).  stage = -1 selects
+ *   every head of every rank (n = H, h0 = 0).
+ *
+ * GQA: q head h (index inside the buffer) reads kv head h / G, G = H_q/H_kv.
+ * A stage owns C q heads and C/G kv heads, so C % G == 0 is required.
+ *
+ * Masks (AutoSP paper, section 2.A step 4, index recomputation; TRL SFTTrainer
+ * packing): `cu_seqlens` holds num_docs+1 int32 GLOBAL token offsets rising
+ * from 0 to S (device pointer; NULL = one document).  Row i attends key j iff
+ * both lie in the same document and (causal ? j <= i : true).
+ *
+ * Ownership and execution: every pointer argument is a DEVICE pointer that the
+ * caller allocates and frees (the library allocates no device memory).  All
+ * calls are asynchronous on `stream` (a cudaStream_t passed as void*; NULL is
+ * the legacy default stream) and return a status code; the message for the
+ * last failure on the calling thread is ulysses_last_error().
+ *
+ * Errors: ULYSSES_ERR_INVALID for shapes the method rejects (S % P != 0,
+ * H % P != 0 — the pages' "num_heads >= sp_size, divisible" constraint —,
+ * hq % C != 0, C % G != 0, bad stage, NULL pointers, in-place re-layout);
+ * ULYSSES_ERR_UNSUPPORTED for valid but unimplemented cases (D not in {64,128},
+ * B > 1 together with cu_seqlens); ULYSSES_ERR_CUDA when a launch fails;
+ * ULYSSES_ERR_TIMEOUT (from ulysses_check) when a kernel gave up a bounded wait.
+ * cu_seqlens contents are validated on the device: a non-monotone table or
+ * one that does not end at S sets the device error word (read by
+ * ulysses_check) and the attention kernels then write nothing meaningful.
+ */
+#ifndef ULYSSES_H
+#define ULYSSES_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+  ULYSSES_OK = 0,
+  ULYSSES_ERR_INVALID = 1,
+  ULYSSES_ERR_UNSUPPORTED = 2,
+  ULYSSES_ERR_CUDA = 3,
+  ULYSSES_ERR_TIMEOUT = 4,
+  ULYSSES_ERR_BAD_SEQLENS = 5
+};
+
+enum { ULYSSES_BF16 = 0, ULYSSES_FP32 = 1 };
+
+/* Kernel selection for diagnostics: AUTO picks the tcgen05 kernels for BF16
+ * with D = 128 and the fp32 SIMT kernels otherwise; SIMT forces the latter. */
+enum { ULYSSES_KERNEL_AUTO = 0, ULYSSES_KERNEL_SIMT = 1 };
+
+/* ---------------------------------------------------------------------------
+ * All-to-all #1 (step 3): sequence layout -> head layout of one stage.
+ *   x_seq   [B][S][H][D], read only.
+ *   x_head  [B][n][S][D], written (n = head_chunk, or H when stage = -1).
+ *   H       heads of THIS tensor (H_q for Q/O/dO, H_kv for K/V).
+ *   head_chunk  heads of this tensor per stage per rank (C for Q, C/G for K/V);
+ *           ignored when stage = -1.
+ *   dtype   ULYSSES_BF16 or ULYSSES_FP32 (only the element size matters: the
+ *           copy is bit-exact).
+ * x_seq and x_head must not overlap.  Both must be 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+int ulysses_seq2head(const void* x_seq, void* x_head, int64_t S, int B, int H, int D, int P,
+                     int head_chunk, int stage, int dtype, void* stream);
+
+/* All-to-all #2 (step 5): head layout of one stage -> its heads of the
+ * sequence layout.  Arguments as ulysses_seq2head; only the selected stage's
+ * heads of x_seq are written. */
+int ulysses_head2seq(const void* x_head, void* x_seq, int64_t S, int B, int H, int D, int P,
+                     int head_chunk, int stage, int dtype, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Local attention forward (step 4) on head-layout buffers of one stage.
+ *   q_h  [B][Cq][S][D],  k_h, v_h [B][Cq/G][S][D]   (Cq = head_chunk, or H_q
+ *        when stage = -1), dtype BF16 or FP32.
+ *   o_h  [B][Cq][S][D] written in the input dtype: O_i = sum_j softmax(s_i)_j v_j
+ *   lse  [B][Cq][S] fp32 written: natural-log logsumexp of the scaled scores.
+ *   scale  score scale; <= 0 selects 1/sqrt(D).
+ * All of q_h/k_h/v_h/o_h must be 16-byte aligned.
+ * ------------------------------------------------------------------------- */
+int ulysses_attn_fwd(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse,
+                     int64_t S, int B, int H_q, int H_kv, int D, int P, int head_chunk, int stage,
+                     const int32_t* cu_seqlens, int num_docs, int causal, float scale, int dtype,
+                     void* stream);
+
+/* Bytes of device workspace ulysses_attn_bwd needs (the per-row
+ * D_i = dO_i . O_i terms, fp32, plus alignment). */
+size_t ulysses_attn_bwd_workspace(int64_t S, int B, int H_q, int H_kv, int D, int P,
+                                  int head_chunk, int stage, int dtype);
+
+/* ---------------------------------------------------------------------------
+ * Local attention backward on head-layout buffers of one stage (the adjoint of
+ * step 4; the adjoint of each all-to-all is the other one).
+ *   inputs  q_h, k_h, v_h, o_h (forward output), do_h [B][Cq][S][D], lse (from
+ *           the forward), all as in ulysses_attn_fwd.
+ *   outputs dq_h [B][Cq][S][D], dk_h, dv_h [B][Cq/G][S][D], all fp32,
+ *           overwritten.  dK/dV are summed over the G q heads of each kv head.
+ *   workspace  device scratch of at least ulysses_attn_bwd_workspace() bytes,
+ *           256-byte aligned, owned by the caller; contents need no init.
+ * ------------------------------------------------------------------------- */
+int ulysses_attn_bwd(const void* q_h, const void* k_h, const void* v_h, const void* o_h,
+                     const void* do_h, const float* lse, float* dq_h, float* dk_h, float* dv_h,
+                     void* workspace, size_t ws_bytes, int64_t S, int B, int H_q, int H_kv, int D,
+                     int P, int head_chunk, int stage, const int32_t* cu_seqlens, int num_docs,
+                     int causal, float scale, int dtype, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Whole layer (steps 3-5, forward or backward) with the UPipe stage loop run
+ * natively: for every rank r and chunk c, seq2head of the stage's Q/K/V
+ * (and O/dO), attention, head2seq of the results.  Head-layout buffers of one
+ * stage live in `workspace` and are reused by the next stage, which bounds the
+ * attention-side scratch by the chunk size.
+ *   q_seq/o_seq/do_seq [B][S][H_q][D], k_seq/v_seq [B][S][H_kv][D] (dtype)
+ *   lse  [B][H_q][S] fp32 (global head order), written by fwd, read by bwd
+ *   dq_seq [B][S][H_q][D], dk_seq/dv_seq [B][S][H_kv][D], fp32, written by bwd
+ *   workspace  >= ulysses_layer_workspace() bytes, 256-byte aligned.
+ * ------------------------------------------------------------------------- */
+size_t ulysses_layer_workspace(int64_t S, int B, int H_q, int H_kv, int D, int P, int head_chunk,
+                               int dtype);
+
+int ulysses_layer_fwd(const void* q_seq, const void* k_seq, const void* v_seq, void* o_seq,
+                      float* lse, int64_t S, int B, int H_q, int H_kv, int D, int P,
+                      int head_chunk, const int32_t* cu_seqlens, int num_docs, int causal,
+                      float scale, int dtype, void* workspace, size_t ws_bytes, void* stream);
+
+int ulysses_layer_bwd(const void* q_seq, const void* k_seq, const void* v_seq, const void* o_seq,
+                      const void* do_seq, const float* lse, float* dq_seq, float* dk_seq,
+                      float* dv_seq, int64_t S, int B, int H_q, int H_kv, int D, int P,
+                      int head_chunk, const int32_t* cu_seqlens, int num_docs, int causal,
+                      float scale, int dtype, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Status and diagnostics.
+ * ulysses_check: synchronises `stream`, then reads and clears the device
+ *   error word that kernels set when a bounded wait expires (returns
+ *   ULYSSES_ERR_TIMEOUT) or when cu_seqlens is malformed
+ *   (ULYSSES_ERR_BAD_SEQLENS).  Returns ULYSSES_ERR_CUDA if the stream
+ *   reports a CUDA error.
+ * ulysses_last_error: message of the last failure on this thread ("" if none).
+ * ulysses_set_kernel: ULYSSES_KERNEL_AUTO or ULYSSES_KERNEL_SIMT (process wide).
+ * ulysses_launch_count: number of kernels this library has launched so far in
+ *   this process (host-side counter).
+ * ------------------------------------------------------------------------- */
+int ulysses_check(void* stream);
+const char* ulysses_last_error(void);
+int ulysses_set_kernel(int which);
+long long ulysses_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ULYSSES_H */

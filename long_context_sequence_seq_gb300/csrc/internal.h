@@ -1,0 +1,33 @@
+// Internal launcher interfaces shared by the CUDA translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ulysses {
+
+// Arguments of one attention launch on head-layout buffers (batch folded into
+// the head index: buffer q head n in [0, n_q) reads kv head n / G).
+struct AttnArgs {
+  const void* q; const void* k; const void* v; const void* o; const void* dO;
+  void* o_out;          // forward output O (input dtype)
+  float* lse;           // forward output LSE
+  const float* lse_in;  // backward input LSE
+  float* dq; float* dk; float* dv;
+  float* delta;         // backward scratch D_i, [n_q][S]
+  int64_t S;
+  int n_q;              // q heads in the buffer across the batch (B * nq)
+  int nq;               // q heads per batch entry in the buffer
+  int G; int D;
+  int64_t lse_bstride;  // LSE element stride between batch entries
+  const int32_t* cu; int nd; int causal; float scale; int dtype;
+};
+
+int launch_relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, int D,
+                    int n, int h0, int elt, cudaStream_t stream);
+int launch_simt_fwd(const AttnArgs& a, cudaStream_t st);
+int launch_simt_bwd(const AttnArgs& a, cudaStream_t st);
+int launch_delta(const AttnArgs& a, cudaStream_t st);
+int launch_check_seqlens(const int32_t* cu, int nd, int64_t S, cudaStream_t st);
+
+}  // namespace ulysses

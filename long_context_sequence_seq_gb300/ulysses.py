@@ -1,0 +1,233 @@
+"""Thin ctypes binding over libulysses.so (argument marshalling only).
+
+Every step of the path runs in the library's CUDA kernels; this module only
+checks tensor properties, allocates outputs through PyTorch and passes raw
+device pointers and the current CUDA stream.  Importing it does not load the
+library; the first call does, and fails loudly if the library is missing.
+
+Layouts: sequence layout [B, S, H, D] (P stacked rank chunks of S/P tokens),
+head layout [B, n, S, D] (the n heads of one UPipe stage, or all heads).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libulysses.so")
+
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_SEQLENS = range(6)
+BF16, FP32 = 0, 1
+KERNEL_AUTO, KERNEL_SIMT = 0, 1
+
+_lib = None
+
+
+class UlyssesError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"ulysses error {code}: {msg}")
+        self.code = code
+
+
+def lib():
+    """Load libulysses.so (built by ``build.build()``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "long_context_sequence_seq_gb300.build.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.ulysses_seq2head.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
+    L.ulysses_head2seq.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
+    L.ulysses_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, i32,
+                                   vp, i32, i32, f32, i32, vp]
+    L.ulysses_attn_bwd_workspace.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32]
+    L.ulysses_attn_bwd_workspace.restype = sz
+    L.ulysses_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i32, i32,
+                                   i32, i32, i32, i32, i32, vp, i32, i32, f32, i32, vp]
+    L.ulysses_layer_workspace.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32]
+    L.ulysses_layer_workspace.restype = sz
+    L.ulysses_layer_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, vp,
+                                    i32, i32, f32, i32, vp, sz, vp]
+    L.ulysses_layer_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32,
+                                    i32, i32, vp, i32, i32, f32, i32, vp, sz, vp]
+    L.ulysses_check.argtypes = [vp]
+    L.ulysses_last_error.restype = ctypes.c_char_p
+    L.ulysses_set_kernel.argtypes = [i32]
+    L.ulysses_launch_count.restype = ctypes.c_longlong
+    _lib = L
+    return L
+
+
+def _ck(rc):
+    if rc != OK:
+        raise UlyssesError(rc, lib().ulysses_last_error().decode())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return FP32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _cu(cu_seqlens):
+    if cu_seqlens is None:
+        return None, 0
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    return _p(cu_seqlens), cu_seqlens.numel() - 1
+
+
+def _stage(stage):
+    return -1 if stage is None else int(stage)
+
+
+# --------------------------------------------------------------- re-layout
+
+def seq2head(x_seq, P, head_chunk=None, stage=None, out=None, stream=None):
+    """All-to-all #1: [B,S,H,D] -> [B,n,S,D] for the stage (all heads if None)."""
+    B, S, H, D = x_seq.shape
+    n = H if stage is None else head_chunk
+    if out is None:
+        out = torch.empty((B, n, S, D), dtype=x_seq.dtype, device=x_seq.device)
+    _ck(lib().ulysses_seq2head(_p(x_seq), _p(out), S, B, H, D, P, head_chunk or 0,
+                               _stage(stage), _dtype_code(x_seq), _stream(stream)))
+    return out
+
+
+def head2seq(x_head, x_seq, P, head_chunk=None, stage=None, stream=None):
+    """All-to-all #2: write [B,n,S,D] into the stage's heads of [B,S,H,D]."""
+    B, S, H, D = x_seq.shape
+    if x_head.dtype != x_seq.dtype:
+        raise TypeError("dtype mismatch")
+    _ck(lib().ulysses_head2seq(_p(x_head), _p(x_seq), S, B, H, D, P, head_chunk or 0,
+                               _stage(stage), _dtype_code(x_seq), _stream(stream)))
+    return x_seq
+
+
+# --------------------------------------------------------------- attention
+
+def attn_fwd(q_h, k_h, v_h, H_q, H_kv, P, head_chunk=None, stage=None, cu_seqlens=None,
+             causal=True, scale=None, out=None, lse=None, stream=None):
+    """Local attention on head-layout buffers: returns (O [B,n,S,D], LSE [B,n,S])."""
+    B, n, S, D = q_h.shape
+    if out is None:
+        out = torch.empty_like(q_h)
+    if lse is None:
+        lse = torch.empty((B, n, S), dtype=torch.float32, device=q_h.device)
+    cp, nd = _cu(cu_seqlens)
+    _ck(lib().ulysses_attn_fwd(_p(q_h), _p(k_h), _p(v_h), _p(out), _p(lse), S, B, H_q, H_kv, D, P,
+                               head_chunk or 0, _stage(stage), cp, nd, int(bool(causal)),
+                               float(scale or 0.0), _dtype_code(q_h), _stream(stream)))
+    return out, lse
+
+
+def attn_bwd_workspace_bytes(S, B, H_q, H_kv, D, P, head_chunk=None, stage=None, dtype=BF16):
+    return lib().ulysses_attn_bwd_workspace(S, B, H_q, H_kv, D, P, head_chunk or 0,
+                                            _stage(stage), dtype)
+
+
+def attn_bwd(q_h, k_h, v_h, o_h, do_h, lse, H_q, H_kv, P, head_chunk=None, stage=None,
+             cu_seqlens=None, causal=True, scale=None, workspace=None, dq=None, dk=None, dv=None,
+             stream=None):
+    """Backward on head-layout buffers: returns fp32 (dQ, dK, dV)."""
+    B, n, S, D = q_h.shape
+    dev = q_h.device
+    dq = torch.empty(q_h.shape, dtype=torch.float32, device=dev) if dq is None else dq
+    dk = torch.empty(k_h.shape, dtype=torch.float32, device=dev) if dk is None else dk
+    dv = torch.empty(v_h.shape, dtype=torch.float32, device=dev) if dv is None else dv
+    ws_b = attn_bwd_workspace_bytes(S, B, H_q, H_kv, D, P, head_chunk, stage, _dtype_code(q_h))
+    if workspace is None:
+        workspace = torch.empty(max(ws_b, 256), dtype=torch.uint8, device=dev)
+    cp, nd = _cu(cu_seqlens)
+    _ck(lib().ulysses_attn_bwd(_p(q_h), _p(k_h), _p(v_h), _p(o_h), _p(do_h), _p(lse), _p(dq),
+                               _p(dk), _p(dv), _p(workspace), workspace.numel(), S, B, H_q, H_kv,
+                               D, P, head_chunk or 0, _stage(stage), cp, nd, int(bool(causal)),
+                               float(scale or 0.0), _dtype_code(q_h), _stream(stream)))
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------- whole layer
+
+def layer_workspace_bytes(S, B, H_q, H_kv, D, P, head_chunk, dtype=BF16):
+    return lib().ulysses_layer_workspace(S, B, H_q, H_kv, D, P, head_chunk, dtype)
+
+
+def layer_workspace(S, B, H_q, H_kv, D, P, head_chunk, dtype=BF16, device="cuda"):
+    n = layer_workspace_bytes(S, B, H_q, H_kv, D, P, head_chunk, dtype)
+    if n == 0:
+        raise UlyssesError(ERR_INVALID, "invalid layer shape")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def layer_fwd(q_seq, k_seq, v_seq, P, head_chunk, cu_seqlens=None, causal=True, scale=None,
+              workspace=None, out=None, lse=None, stream=None):
+    """Steps 3-5 with the UPipe stage loop: returns (O [B,S,H_q,D], LSE [B,H_q,S])."""
+    B, S, H_q, D = q_seq.shape
+    H_kv = k_seq.shape[2]
+    dt = _dtype_code(q_seq)
+    if workspace is None:
+        workspace = layer_workspace(S, B, H_q, H_kv, D, P, head_chunk, dt, q_seq.device)
+    out = torch.empty_like(q_seq) if out is None else out
+    lse = torch.empty((B, H_q, S), dtype=torch.float32, device=q_seq.device) if lse is None else lse
+    cp, nd = _cu(cu_seqlens)
+    _ck(lib().ulysses_layer_fwd(_p(q_seq), _p(k_seq), _p(v_seq), _p(out), _p(lse), S, B, H_q, H_kv,
+                                D, P, head_chunk, cp, nd, int(bool(causal)), float(scale or 0.0),
+                                dt, _p(workspace), workspace.numel(), _stream(stream)))
+    return out, lse
+
+
+def layer_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, P, head_chunk, cu_seqlens=None,
+              causal=True, scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """Backward of the layer: returns fp32 (dQ, dK, dV) in sequence layout."""
+    B, S, H_q, D = q_seq.shape
+    H_kv = k_seq.shape[2]
+    dt = _dtype_code(q_seq)
+    dev = q_seq.device
+    if workspace is None:
+        workspace = layer_workspace(S, B, H_q, H_kv, D, P, head_chunk, dt, dev)
+    dq = torch.empty(q_seq.shape, dtype=torch.float32, device=dev) if dq is None else dq
+    dk = torch.empty(k_seq.shape, dtype=torch.float32, device=dev) if dk is None else dk
+    dv = torch.empty(v_seq.shape, dtype=torch.float32, device=dev) if dv is None else dv
+    cp, nd = _cu(cu_seqlens)
+    _ck(lib().ulysses_layer_bwd(_p(q_seq), _p(k_seq), _p(v_seq), _p(o_seq), _p(do_seq), _p(lse),
+                                _p(dq), _p(dk), _p(dv), S, B, H_q, H_kv, D, P, head_chunk, cp, nd,
+                                int(bool(causal)), float(scale or 0.0), dt, _p(workspace),
+                                workspace.numel(), _stream(stream)))
+    return dq, dk, dv
+
+
+# --------------------------------------------------------------- diagnostics
+
+def check(stream=None):
+    """Synchronise and raise if a kernel flagged a timeout or bad cu_seqlens."""
+    _ck(lib().ulysses_check(_stream(stream)))
+
+
+def set_kernel(which: int):
+    _ck(lib().ulysses_set_kernel(which))
+
+
+def launch_count() -> int:
+    return int(lib().ulysses_launch_count())

@@ -1,0 +1,86 @@
+"""Host-side checks of the C ABI library (no GPU needed): it builds, loads,
+exports every symbol include/ulysses.h declares, and rejects invalid shapes
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from long_context_sequence_seq_gb300 import build as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    return B.build()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ulysses.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ulysses_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(libpath):
+    lib = ctypes.CDLL(libpath)
+    names = _declared()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_loads(libpath):
+    from long_context_sequence_seq_gb300 import ulysses
+    L = ulysses.lib()
+    assert L.ulysses_launch_count() >= 0
+
+
+def test_host_validation_without_device(libpath):
+    from long_context_sequence_seq_gb300 import ulysses as U
+    L = U.lib()
+    dummy = ctypes.c_void_p(256)
+    # S % P != 0
+    assert L.ulysses_seq2head(dummy, ctypes.c_void_p(1 << 20), 30, 1, 8, 128, 4, 2, 0, U.BF16, None) == U.ERR_INVALID
+    # heads not divisible by P (num_heads >= sp_size and divisible)
+    assert L.ulysses_seq2head(dummy, ctypes.c_void_p(1 << 20), 32, 1, 6, 128, 4, 1, 0, U.BF16, None) == U.ERR_INVALID
+    # head_chunk not dividing H/P
+    assert L.ulysses_seq2head(dummy, ctypes.c_void_p(1 << 20), 32, 1, 8, 128, 2, 3, 0, U.BF16, None) == U.ERR_INVALID
+    # stage out of range
+    assert L.ulysses_seq2head(dummy, ctypes.c_void_p(1 << 20), 32, 1, 8, 128, 2, 2, 4, U.BF16, None) == U.ERR_INVALID
+    # in place
+    assert L.ulysses_seq2head(dummy, dummy, 32, 1, 8, 128, 2, 2, 0, U.BF16, None) == U.ERR_INVALID
+    # unaligned
+    assert L.ulysses_seq2head(ctypes.c_void_p(264), ctypes.c_void_p(1 << 20), 32, 1, 8, 128, 2, 2, 0, U.BF16, None) == U.ERR_INVALID
+    args = [dummy] * 5
+    # attention: C % G != 0 (a stage must own whole kv heads)
+    rc = L.ulysses_attn_fwd(*args, 64, 1, 32, 8, 128, 4, 2, 0, None, 0, 1, 0.0, U.BF16, None)
+    assert rc == U.ERR_INVALID
+    # D unsupported
+    rc = L.ulysses_attn_fwd(*args, 64, 1, 32, 8, 96, 4, 8, 0, None, 0, 1, 0.0, U.BF16, None)
+    assert rc == U.ERR_UNSUPPORTED
+    # cu_seqlens with B > 1
+    rc = L.ulysses_attn_fwd(*args, 64, 2, 32, 8, 128, 4, 8, 0, dummy, 1, 1, 0.0, U.BF16, None)
+    assert rc == U.ERR_UNSUPPORTED
+    # H_q not multiple of H_kv
+    rc = L.ulysses_attn_fwd(*args, 64, 1, 12, 8, 128, 4, 3, 0, None, 0, 1, 0.0, U.BF16, None)
+    assert rc == U.ERR_INVALID
+    assert b"kv" in L.ulysses_last_error() or len(L.ulysses_last_error()) > 0
+    # empty input is a no-op, never a launch
+    before = L.ulysses_launch_count()
+    assert L.ulysses_seq2head(dummy, ctypes.c_void_p(1 << 20), 0, 1, 8, 128, 2, 2, 0, U.BF16, None) == U.OK
+    assert L.ulysses_attn_fwd(*args, 0, 1, 32, 8, 128, 4, 8, 0, None, 0, 1, 0.0, U.BF16, None) == U.OK
+    assert L.ulysses_launch_count() == before
+
+
+def test_workspace_sizes(libpath):
+    from long_context_sequence_seq_gb300 import ulysses as U
+    S = 65536
+    ws = U.attn_bwd_workspace_bytes(S, 1, 32, 8, 128, 4, 8, 0)
+    assert ws == 8 * S * 4
+    lw = U.layer_workspace_bytes(S, 1, 32, 8, 128, 4, 8)
+    # per stage: q,o,dO (bf16) + k,v (bf16) + dq (fp32) + dk,dv (fp32) + delta
+    want = 3 * 8 * S * 128 * 2 + 2 * 2 * S * 128 * 2 + 8 * S * 128 * 4 + 2 * 2 * S * 128 * 4 + 8 * S * 4
+    assert lw == want
+    assert U.layer_workspace_bytes(S, 1, 32, 8, 128, 4, 3) == 0
