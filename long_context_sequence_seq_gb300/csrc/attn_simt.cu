@@ -37,11 +37,6 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
-__device__ __forceinline__ int64_t lse_index(int64_t n, int nq, int64_t lse_bstride, int64_t S,
-                                             int64_t t) {
-  return (n / nq) * lse_bstride + (n % nq) * S + t;
-}
-
 // Load rows [r0, r0+rows) of a [S][D] matrix into shared fp32 [rows][ld], zero past S.
 template <typename T, int D>
 __device__ __forceinline__ void load_rows(float* dst, int ld, const T* __restrict__ src, int64_t S,

@@ -72,6 +72,12 @@ __device__ __forceinline__ int doc_of(const int32_t* __restrict__ cu, int nd, in
   return lo;
 }
 
+// LSE element of buffer head n (batch folded into n), token t.
+__device__ __forceinline__ int64_t lse_index(int64_t n, int nq, int64_t lse_bstride, int64_t S,
+                                             int64_t t) {
+  return (n / nq) * lse_bstride + (n % nq) * S + t;
+}
+
 // Key range [lo, hi) of query row i.
 __device__ __forceinline__ void key_range(const int32_t* __restrict__ cu, int nd, int64_t S,
                                           int causal, int64_t i, int64_t& lo, int64_t& hi) {

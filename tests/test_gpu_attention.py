@@ -46,7 +46,9 @@ SMALL = [
     # S, Hq, Hkv, D, P, C, dtype, doc lengths (None = one causal doc), causal
     (1, 2, 1, 128, 1, 2, "bf16", None, True),
     (17, 4, 2, 128, 1, 4, "bf16", None, True),
-    (200, 4, 1, 128, 2, 2, "bf16", None, True),
+    (200, 4, 2, 128, 2, 2, "bf16", None, True),
+    (256, 8, 2, 128, 2, 4, "bf16", None, True),
+    (640, 4, 1, 128, 1, 4, "bf16", [300, 340], True),
     (384, 8, 2, 128, 2, 4, "bf16", [100, 200, 84], True),
     (417, 4, 4, 128, 1, 2, "bf16", [1, 129, 130, 157], True),     # ragged tail, 1-token doc
     (300, 4, 2, 128, 2, 2, "bf16", [150, 150], False),
