@@ -300,7 +300,7 @@ def gpu_arm(args):
     torch.cuda.set_device(dev)
     from long_context_sequence_seq_gb300 import ulysses as U
     U.lib()
-    w = inputs.WORKLOADS[args.workload]
+    w = workload_from_args(args)
     cu_np = inputs.workload_cu_seqlens(w)
     step = LayerStep(w, dev, cu_np)
     for _ in range(args.warmup):
@@ -336,10 +336,13 @@ def gpu_arm(args):
     fl_fwd, fl_bwd = 4.0 * w.D * pairs, 10.0 * w.D * pairs
     t_fwd, t_bwd = statistics.mean(fwd_t), statistics.mean(bwd_t)
     hbm, bf16, bf16_sus, peak_src = load_peaks()
-    relay_gbs, _ = measure_relayout(w, dev)
+    relay_gbs = None
+    e2e = None
     del step
     torch.cuda.empty_cache()
-    e2e = e2e_measure(w, dev, cu_np, max(1, args.steps // 2), max(1, args.warmup // 2))
+    if not args.kernels_only:
+        relay_gbs, _ = measure_relayout(w, dev)
+        e2e = e2e_measure(w, dev, cu_np, max(1, args.steps // 2), max(1, args.warmup // 2))
     # dominant kernel = attention backward (2.5x the forward's FLOPs)
     bwd_per_launch_s = t_bwd / n_launch_attn
     achieved = fl_bwd / n_launch_attn / bwd_per_launch_s / 1e12
@@ -356,7 +359,7 @@ def gpu_arm(args):
         "attn_fwd_ms": t_fwd * 1e3, "attn_bwd_ms": t_bwd * 1e3,
         "attn_fwd_tflops": fl_fwd / t_fwd / 1e12, "attn_bwd_tflops": fl_bwd / t_bwd / 1e12,
         "frac_fwd_bwd_of_bf16_peak": (fl_fwd + fl_bwd) / (t_fwd + t_bwd) / 1e12 / bf16,
-        "relayout_gbs": relay_gbs, "relayout_frac_hbm": relay_gbs / hbm,
+        "relayout_gbs": relay_gbs, "relayout_frac_hbm": None if relay_gbs is None else relay_gbs / hbm,
         "relayout_bytes_per_step": relayout_bytes_per_step(w),
         "roofline": {"kernel": "attn_bwd", "bound": "tensor", "achieved": achieved,
                      "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16, "traffic": None,
@@ -380,7 +383,7 @@ def reference_arm(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
-    w = inputs.WORKLOADS[args.workload]
+    w = workload_from_args(args)
     cu_np = inputs.workload_cu_seqlens(w)
     for _ in range(args.warmup):
         cpu_baseline(w, cu_np, budget_s=2.0)
@@ -402,6 +405,14 @@ def reference_arm(args):
     print(json.dumps(res), flush=True)
 
 
+def workload_from_args(args):
+    w = inputs.WORKLOADS[args.workload]
+    if args.seq_len:
+        import dataclasses
+        w = dataclasses.replace(w, name=f"{w.name}@S={args.seq_len}", S=args.seq_len)
+    return w
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -410,6 +421,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="qwen3_4b_64k", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernels-only", action="store_true",
+                    help="skip the isolated re-layout and end-to-end measurements (profiling runs)")
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override S of the workload (smaller profiling cases)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

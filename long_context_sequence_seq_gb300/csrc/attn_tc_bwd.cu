@@ -1,11 +1,438 @@
-// K4: tcgen05 attention backward (placeholder until the kernel lands).
-#include "common.cuh"
+// K3 + K4: attention backward for sm_103a (bf16 inputs, fp32 gradients).
+//
+// The adjoint of step 4 of "How Ulysses sequence parallelism works" (local
+// dense attention): with P recomputed from the saved logsumexp,
+//   P_ij = exp(s_ij - LSE_i),  dV_j = sum_i P_ij dO_i,  dP_ij = dO_i.v_j,
+//   D_i = dO_i.O_i,  dS_ij = P_ij (dP_ij - D_i),
+//   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
+// dK/dV summed over the G query heads of each kv head.
+//
+// K3 (bwd_pre_kernel): D_i for every row and dQ := 0 (dQ is accumulated with
+// fp32 reductions by K4).
+//
+// K4 (tc_bwd_kernel): one CTA per (kv head, 128-key block); it owns dK/dV of
+// its block (accumulated in TMEM, no atomics) and walks the G query heads and
+// every 64-row query block that can see its keys.  Transposed formulation,
+// so the key index is the TMEM lane:
+//   S^T  = K Q_i^T            (M=128 keys, N=64 queries, K=D)
+//   dP^T = V dO_i^T
+//   softmax warps: P^T = exp2(S^T*scale*log2e - LSE_i*log2e), masked;
+//                  dS^T = P^T (dP^T - D_i); both stored back to TMEM as bf16,
+//                  dS^T also to shared memory (swizzled, [key][query]).
+//   dV  += P^T dO_i            (A = P^T from TMEM, B = dO_i, MN-major)
+//   dK  += dS^T Q_i            (A = dS^T from TMEM, B = Q_i, MN-major)
+//   dQ_i^T = K^T dS^T          (M = D, N = 64 queries; A = K, MN-major;
+//                               B = dS^T from shared memory, MN-major)
+// The dQ readout warps (TMEM lane = feature d) add scale * dQ_i^T into the
+// fp32 dQ with coalesced reductions (32 consecutive d per warp instruction).
+//
+// Warp roles (384 threads): 0 TMA producer (+ LSE/D_i loads), 1 TMEM owner and
+// MMA issuer, 4-7 softmax/gradient warps (thread = key row), 8-11 dQ readout
+// (thread = feature).  TMEM columns: dV [0,128), dK [128,256), S^T/P^T
+// [256,320), dP^T/dS^T [320,384), dQ^T [384,448).
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace ulysses {
+
 ULYSSES_ERROR_READER(read_error_attn_tc_bwd)
-bool tc_bwd_supported(const AttnArgs&) { return false; }
-int launch_tc_bwd(const AttnArgs&, cudaStream_t) {
-  return set_error(ULYSSES_ERR_UNSUPPORTED, "tcgen05 backward not built");
+
+namespace {
+
+using namespace tc;
+
+constexpr int BN = 128;     // keys per CTA
+constexpr int BMQ = 64;     // queries per inner tile
+constexpr int D = 128;
+constexpr int NSTAGE = 2;
+constexpr int kThreads = 384;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 320, kColDQ = 384;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct BwdLayout {
+  static constexpr int kChunkKV = BN * 128;          // 64 features x 128 keys
+  static constexpr int kChunkQ = BMQ * 128;          // 64 features x 64 queries
+  static constexpr int kTileKV = kChunkKV * (D / 64);
+  static constexpr int kTileQ = kChunkQ * (D / 64);
+  static constexpr int kK = 0;
+  static constexpr int kV = kK + kTileKV;
+  static constexpr int kQ = kV + kTileKV;                    // NSTAGE tiles
+  static constexpr int kDO = kQ + NSTAGE * kTileQ;            // NSTAGE tiles
+  static constexpr int kDS = kDO + NSTAGE * kTileQ;           // [128 keys][64 queries] bf16
+  static constexpr int kStat = kDS + BN * BMQ * 2;            // NSTAGE x {LSE2[64], D[64]}
+  static constexpr int kBar = kStat + NSTAGE * 2 * BMQ * 4;
+  // kv_full, q_full[2], q_empty[2], s_full, ds_full, dq_full, dq_empty, it_done, fin, drain
+  static constexpr int kNumBar = 1 + 2 * NSTAGE + 7;
+  static constexpr int kMisc = kBar + kNumBar * 8;
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
+                                                      const __nv_bfloat16* __restrict__ dO,
+                                                      float* __restrict__ delta,
+                                                      float* __restrict__ dq, int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (row >= rows) return;
+  // 128 features = 32 lanes x 4
+  const uint2 ov = *reinterpret_cast<const uint2*>(o + row * D + lane * 4);
+  const uint2 dv = *reinterpret_cast<const uint2*>(dO + row * D + lane * 4);
+  const __nv_bfloat162* o2 = reinterpret_cast<const __nv_bfloat162*>(&ov);
+  const __nv_bfloat162* d2 = reinterpret_cast<const __nv_bfloat162*>(&dv);
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    float2 a = __bfloat1622float2(o2[e]), b = __bfloat1622float2(d2[e]);
+    s = fmaf(a.x, b.x, s);
+    s = fmaf(a.y, b.y, s);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  if (lane == 0) delta[row] = s;
+  *reinterpret_cast<float4*>(dq + row * D + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                  const float* __restrict__ lse, const float* __restrict__ delta,
+                  float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
+                  int64_t S, int nq, int G, int64_t lse_bstride, const int32_t* __restrict__ cu,
+                  int nd, int causal, float scale) {
+  using L = BwdLayout;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sK = smem + L::kK;
+  uint8_t* sV = smem + L::kV;
+  uint8_t* sQ = smem + L::kQ;
+  uint8_t* sDO = smem + L::kDO;
+  uint8_t* sDS = smem + L::kDS;
+  float* sStat = reinterpret_cast<float*>(smem + L::kStat);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
+  uint64_t* kv_full = bars;
+  uint64_t* q_full = bars + 1;
+  uint64_t* q_empty = q_full + NSTAGE;
+  uint64_t* s_full = q_empty + NSTAGE;
+  uint64_t* ds_full = s_full + 1;
+  uint64_t* dq_full = ds_full + 1;
+  uint64_t* dq_empty = dq_full + 1;
+  uint64_t* it_done = dq_empty + 1;
+  uint64_t* fin = it_done + 1;
+  uint64_t* drain = fin + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kvh = blockIdx.x;                          // kv head in the buffer
+  const int64_t k0 = (int64_t)blockIdx.y * BN;         // first key of the block
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < NSTAGE; ++s) { mbar_init(&q_full[s], 1); mbar_init(&q_empty[s], 1); }
+    mbar_init(s_full, 1);
+    mbar_init(ds_full, 4);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_empty, 4);
+    mbar_init(it_done, 1);
+    mbar_init(fin, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&tmQ); tma_prefetch(&tmK); tma_prefetch(&tmV); tma_prefetch(&tmDO);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  // Query rows that can see this key block: [q_lo, q_hi), q_lo rounded down
+  // to the query tile so every tile starts on a 64-row boundary.
+  const int64_t last_key = (k0 + BN < S ? k0 + BN : S) - 1;
+  int64_t q_lo, q_hi, tmp;
+  query_range(cu, nd, S, causal, k0, q_lo, tmp);
+  query_range(cu, nd, S, causal, last_key, tmp, q_hi);
+  q_lo = (q_lo / BMQ) * BMQ;
+  const int n_qb = q_hi > q_lo ? (int)((q_hi - q_lo + BMQ - 1) / BMQ) : 0;
+  const int n_it = n_qb * G;   // iteration it -> q head g = it / n_qb, block qb = it % n_qb
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      mbar_expect_tx(kv_full, 2 * L::kTileKV);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(sK + c * L::kChunkKV, &tmK, c * 64, (int)k0, kvh, kv_full);
+        tma_load_3d(sV + c * L::kChunkKV, &tmV, c * 64, (int)k0, kvh, kv_full);
+      }
+    }
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % NSTAGE;
+      const uint32_t round = it / NSTAGE;
+      if (!mbar_wait(&q_empty[st], (round & 1) ^ 1, abort_flag)) break;
+      const int n = kvh * G + it / n_qb;
+      const int64_t q0 = q_lo + (int64_t)(it % n_qb) * BMQ;
+      // LSE (log2 units) and D_i of the tile's 64 query rows; rows past S get 0
+      float* stat = sStat + st * 2 * BMQ;
+      for (int r = lane; r < BMQ; r += 32) {
+        const int64_t i = q0 + r;
+        stat[r] = i < S ? lse[lse_index(n, nq, lse_bstride, S, i)] * kLog2e : 0.f;
+        stat[BMQ + r] = i < S ? delta[(int64_t)n * S + i] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_expect_tx(&q_full[st], 2 * L::kTileQ);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(sQ + st * L::kTileQ + c * L::kChunkQ, &tmQ, c * 64, (int)q0, n, &q_full[st]);
+          tma_load_3d(sDO + st * L::kTileQ + c * L::kChunkQ, &tmDO, c * 64, (int)q0, n, &q_full[st]);
+        }
+      }
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t id_s = idesc_bf16(BN, BMQ, false, false);    // S^T, dP^T
+    constexpr uint32_t id_g = idesc_bf16(BN, D, false, true);       // dV, dK
+    constexpr uint32_t id_q = idesc_bf16(D, BMQ, true, true);       // dQ^T
+    const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ds_addr = smem_u32(sDS);
+    bool ok = mbar_wait(kv_full, 0, abort_flag);
+    for (int it = 0; ok && it < n_it; ++it) {
+      const int st = it % NSTAGE;
+      const uint32_t round = it / NSTAGE;
+      if (!mbar_wait(&q_full[st], round & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t q_addr = smem_u32(sQ + st * L::kTileQ);
+      const uint32_t do_addr = smem_u32(sDO + st * L::kTileQ);
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_kv = (kk >> 2) * L::kChunkKV + (kk & 3) * 32;
+          const uint32_t off_q = (kk >> 2) * L::kChunkQ + (kk & 3) * 32;
+          mma_ss(tbase + kColS, sdesc_sw128(k_addr + off_kv, 16, 1024),
+                 sdesc_sw128(q_addr + off_q, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off_kv = (kk >> 2) * L::kChunkKV + (kk & 3) * 32;
+          const uint32_t off_q = (kk >> 2) * L::kChunkQ + (kk & 3) * 32;
+          mma_ss(tbase + kColDP, sdesc_sw128(v_addr + off_kv, 16, 1024),
+                 sdesc_sw128(do_addr + off_q, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(s_full);
+      }
+      __syncwarp();
+      if (!mbar_wait(ds_full, it & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      if (lane == 0) {
+        // B = dO_i / Q_i as MN-major: 16 queries per step (2048 B), 64-feature
+        // chunks L::kChunkQ apart.
+#pragma unroll
+        for (int kk = 0; kk < BMQ / 16; ++kk) {
+          mma_ts(tbase + kColDV, tbase + kColS + kk * 8, sdesc_sw128(do_addr + kk * 2048, L::kChunkQ, 1024),
+                 id_g, (it > 0 || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < BMQ / 16; ++kk) {
+          mma_ts(tbase + kColDK, tbase + kColDP + kk * 8, sdesc_sw128(q_addr + kk * 2048, L::kChunkQ, 1024),
+                 id_g, (it > 0 || kk > 0) ? 1u : 0u);
+        }
+      }
+      __syncwarp();
+      if (it > 0 && !mbar_wait(dq_empty, (it - 1) & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      if (lane == 0) {
+        // A = K^T (MN-major: 64-feature chunks L::kChunkKV apart), B = dS^T
+        // ([key][query] rows of 128 B); 16 keys per step.
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          mma_ss(tbase + kColDQ, sdesc_sw128(k_addr + kk * 2048, L::kChunkKV, 1024),
+                 sdesc_sw128(ds_addr + kk * 2048, 8192, 1024), id_q, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(dq_full);
+        mma_commit(&q_empty[st]);
+        mma_commit(it_done);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      mma_commit(fin);
+      mma_commit(drain);
+    }
+    __syncwarp();
+    mbar_wait(drain, 0, nullptr);
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ gradient warps
+    const int wq = warp & 3;
+    const int jr = wq * 32 + lane;               // key row in the block = TMEM lane
+    const int64_t j = k0 + jr;
+    int64_t qlo = 0, qhi = 0;
+    if (j < S) query_range(cu, nd, S, causal, j, qlo, qhi);
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const float sl2 = scale * kLog2e;
+    bool ok = true;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % NSTAGE;
+      const uint32_t round = it / NSTAGE;
+      const int64_t q0 = q_lo + (int64_t)(it % n_qb) * BMQ;
+      if (!mbar_wait(&q_full[st], round & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(s_full, it & 1, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const float* stat = sStat + st * 2 * BMQ;
+      const bool full = (q0 >= qlo) && (q0 + BMQ <= qhi);
+      uint32_t pp[32], dd[32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t sv[32], pv[32];
+        tmem_ld32(tbase + lane_off + kColS + c * 32, sv);
+        tmem_ld32(tbase + lane_off + kColDP + c * 32, pv);
+        tmem_ld_wait();
+        reg_fence(sv);
+        reg_fence(pv);
+#pragma unroll
+        for (int e4 = 0; e4 < 32; e4 += 4) {
+          const int col = c * 32 + e4;
+          const float4 l4 = *reinterpret_cast<const float4*>(stat + col);
+          const float4 d4 = *reinterpret_cast<const float4*>(stat + BMQ + col);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+          float p[4], g[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            p[u] = ex2(fmaf(__uint_as_float(sv[e4 + u]), sl2, -lv[u]));
+            if (!full) {
+              const int64_t i = q0 + col + u;
+              p[u] = (i >= qlo && i < qhi) ? p[u] : 0.f;
+            }
+            g[u] = p[u] * (__uint_as_float(pv[e4 + u]) - dl[u]);
+          }
+          pp[col >> 1] = pack_bf16(p[0], p[1]);
+          pp[(col >> 1) + 1] = pack_bf16(p[2], p[3]);
+          dd[col >> 1] = pack_bf16(g[0], g[1]);
+          dd[(col >> 1) + 1] = pack_bf16(g[2], g[3]);
+        }
+      }
+      tmem_st32(tbase + lane_off + kColS, pp);
+      tmem_st32(tbase + lane_off + kColDP, dd);
+      // the previous iteration's dQ^T MMA must be done reading dS^T
+      if (it > 0 && !mbar_wait(it_done, (it - 1) & 1, abort_flag)) { ok = false; break; }
+      uint8_t* row = sDS + jr * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 w = make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]);
+        *reinterpret_cast<uint4*>(row + ((c ^ (jr & 7)) << 4)) = w;
+      }
+      fence_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(ds_full);
+    }
+    // epilogue: dV and scale * dK of this key block
+    if (ok && n_it > 0 && mbar_wait(fin, 0, abort_flag)) {
+      tc_fence_after();
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        float* dst = (which == 0 ? dv : dk) + ((int64_t)kvh * S + j) * D;
+        const float mul = which == 0 ? 1.f : scale;
+        const uint32_t col0 = which == 0 ? kColDV : kColDK;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tbase + lane_off + col0 + c * 32, r);
+          tmem_ld_wait();
+          reg_fence(r);
+          if (j < S) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(dst + c * 32 + e) =
+                  make_float4(__uint_as_float(r[e]) * mul, __uint_as_float(r[e + 1]) * mul,
+                              __uint_as_float(r[e + 2]) * mul, __uint_as_float(r[e + 3]) * mul);
+          }
+        }
+      }
+    } else if (n_it == 0 && j < S) {
+      // no query sees these keys: zero gradients
+      for (int c = 0; c < D; c += 4) {
+        *reinterpret_cast<float4*>(dv + ((int64_t)kvh * S + j) * D + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(dk + ((int64_t)kvh * S + j) * D + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ readout
+    const int wq = warp & 3;
+    const int d = wq * 32 + lane;                // feature = TMEM lane of dQ^T
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    for (int it = 0; it < n_it; ++it) {
+      if (!mbar_wait(dq_full, it & 1, abort_flag)) break;
+      tc_fence_after();
+      uint32_t r[2][32];
+      tmem_ld32(tbase + lane_off + kColDQ, r[0]);
+      tmem_ld32(tbase + lane_off + kColDQ + 32, r[1]);
+      tmem_ld_wait();
+      reg_fence(r[0]);
+      reg_fence(r[1]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_empty);
+      const int n = kvh * G + it / n_qb;
+      const int64_t q0 = q_lo + (int64_t)(it % n_qb) * BMQ;
+      float* base = dq + ((int64_t)n * S + q0) * D + d;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const int col = c * 32 + e;
+          if (q0 + col < S) atomicAdd(base + (int64_t)col * D, __uint_as_float(r[c][e]) * scale);
+        }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool tc_bwd_supported(const AttnArgs& a) {
+  return a.dtype == ULYSSES_BF16 && a.D == 128 && a.S >= BN && (a.S + BN - 1) / BN <= 65535;
+}
+
+int launch_tc_bwd(const AttnArgs& a, cudaStream_t st) {
+  const int64_t rows = (int64_t)a.n_q * a.S;
+  bwd_pre_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(
+      (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, a.delta, a.dq, rows);
+  count_launch();
+  int rc = check_launch("bwd_pre");
+  if (rc) return rc;
+  CUtensorMap tq, tk, tv, tdo;
+  const int n_kv = a.n_q / a.G;
+  if ((rc = make_tmap_bf16_3d(&tq, a.q, a.S, a.n_q, D, BMQ))) return rc;
+  if ((rc = make_tmap_bf16_3d(&tdo, a.dO, a.S, a.n_q, D, BMQ))) return rc;
+  if ((rc = make_tmap_bf16_3d(&tk, a.k, a.S, n_kv, D, BN))) return rc;
+  if ((rc = make_tmap_bf16_3d(&tv, a.v, a.S, n_kv, D, BN))) return rc;
+  const int smem = BwdLayout::kAlloc;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    attr_set = true;
+  }
+  dim3 grid((unsigned)n_kv, (unsigned)((a.S + BN - 1) / BN));
+  tc_bwd_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, a.lse_in, a.delta, a.dq, a.dk, a.dv,
+                                              a.S, a.nq, a.G, a.lse_bstride, a.cu, a.nd, a.causal,
+                                              a.scale);
+  count_launch();
+  return check_launch("tc_bwd");
+}
+
 }  // namespace ulysses
