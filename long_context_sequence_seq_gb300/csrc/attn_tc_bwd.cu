@@ -23,13 +23,15 @@
 //   dK  += dS^T Q_i            (A = dS^T from TMEM, B = Q_i, MN-major)
 //   dQ_i^T = K^T dS^T          (M = D, N = 64 queries; A = K, MN-major;
 //                               B = dS^T from shared memory, MN-major)
-// The dQ readout warps (TMEM lane = feature d) add scale * dQ_i^T into the
-// fp32 dQ with coalesced reductions (32 consecutive d per warp instruction).
+// The gradient warps then read dQ_i^T out of TMEM (lane = feature d), stage
+// scale * dQ_i in shared memory as [query][feature] rows and add the tile's
+// rows into the fp32 dQ with one TMA bulk reduce-add (cp.reduce.async.bulk).
 //
-// Warp roles (384 threads): 0 TMA producer (+ LSE/D_i loads), 1 TMEM owner and
-// MMA issuer, 4-7 softmax/gradient warps (thread = key row), 8-11 dQ readout
-// (thread = feature).  TMEM columns: dV [0,128), dK [128,256), S^T/P^T
-// [256,320), dP^T/dS^T [320,384), dQ^T [384,448).
+// Warp roles (256 threads): 0 TMA producer, 1 TMEM owner and MMA issuer,
+// 2 LSE/D_i loader, 4-7 softmax/gradient warps (thread = key row for P/dS,
+// feature for the dQ readout).  TMEM columns: dV [0,128), dK [128,256), two
+// S^T/P^T buffers [256,384) that also receive each tile's dQ^T, two
+// dP^T/dS^T buffers [384,512).
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -44,10 +46,12 @@ using namespace tc;
 constexpr int BN = 128;     // keys per CTA
 constexpr int BMQ = 64;     // queries per inner tile
 constexpr int D = 128;
-constexpr int NSTAGE = 2;
-constexpr int kThreads = 384;
+constexpr int NSTAGE = 2;   // Q/dO/LSE/D_i ring
+constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 320, kColDQ = 384;
+// TMEM: dV, dK accumulators; two S^T/P^T buffers (each later reused for the
+// tile's dQ^T); two dP^T/dS^T buffers.
+constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct BwdLayout {
@@ -55,15 +59,18 @@ struct BwdLayout {
   static constexpr int kChunkQ = BMQ * 128;          // 64 features x 64 queries
   static constexpr int kTileKV = kChunkKV * (D / 64);
   static constexpr int kTileQ = kChunkQ * (D / 64);
+  static constexpr int kTileDS = BN * BMQ * 2;       // [128 keys][64 queries] bf16
   static constexpr int kK = 0;
   static constexpr int kV = kK + kTileKV;
   static constexpr int kQ = kV + kTileKV;                    // NSTAGE tiles
   static constexpr int kDO = kQ + NSTAGE * kTileQ;            // NSTAGE tiles
-  static constexpr int kDS = kDO + NSTAGE * kTileQ;           // [128 keys][64 queries] bf16
-  static constexpr int kStat = kDS + BN * BMQ * 2;            // NSTAGE x {LSE2[64], D[64]}
+  static constexpr int kDS = kDO + NSTAGE * kTileQ;           // 2 tiles
+  static constexpr int kDQ = kDS + 2 * kTileDS;               // dQ tile staging [64 q][128 d] fp32
+  static constexpr int kStat = kDQ + BMQ * D * 4;             // NSTAGE x {LSE2[64], D[64]}
   static constexpr int kBar = kStat + NSTAGE * 2 * BMQ * 4;
-  // kv_full, q_full[2], q_empty[2], s_full, ds_full, dq_full, dq_empty, it_done, fin, drain
-  static constexpr int kNumBar = 1 + 2 * NSTAGE + 7;
+  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[2], ds_full[2], dsm_free[2],
+  // dq_full[2], dq_empty, fin, drain, stg (gradient-warp group sync)
+  static constexpr int kNumBar = 1 + 2 * NSTAGE + 8 + 4;
   static constexpr int kMisc = kBar + kNumBar * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -94,6 +101,15 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   *reinterpret_cast<float4*>(dq + row * D + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// Pipeline (MMA issue order), it = iteration, b = it & 1:
+//   S^T_{it+1}, dP^T_{it+1}  -> s_full[b']         (needs Q/dO of it+1 and the
+//                                                   readout of dQ^T_{it-1}, which
+//                                                   lived in S buffer b')
+//   wait ds_full[b]  (gradient warps finished tile it)
+//   dV += P^T_it dO_it, dK += dS^T_it Q_it, dQ^T_it = K^T dS^T_it  (into S buffer b)
+//   -> dq_full[b], q_empty[stage], dsm_free[b]
+// so the tensor pipe runs tile it's gradient MMAs and tile it+1's score MMAs
+// while the gradient warps work on tile it+1.
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -116,12 +132,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars + 1;
   uint64_t* q_empty = q_full + NSTAGE;
   uint64_t* s_full = q_empty + NSTAGE;
-  uint64_t* ds_full = s_full + 1;
-  uint64_t* dq_full = ds_full + 1;
-  uint64_t* dq_empty = dq_full + 1;
-  uint64_t* it_done = dq_empty + 1;
-  uint64_t* fin = it_done + 1;
+  uint64_t* ds_full = s_full + 2;
+  uint64_t* dsm_free = ds_full + 2;
+  uint64_t* dq_full = dsm_free + 2;
+  uint64_t* dq_empty = dq_full + 2;
+  uint64_t* fin = dq_empty + 1;
   uint64_t* drain = fin + 1;
+  uint64_t* stg = drain + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -131,14 +148,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < NSTAGE; ++s) { mbar_init(&q_full[s], 1); mbar_init(&q_empty[s], 1); }
-    mbar_init(s_full, 1);
-    mbar_init(ds_full, 4);
-    mbar_init(dq_full, 1);
+    for (int s = 0; s < NSTAGE; ++s) { mbar_init(&q_full[s], 2); mbar_init(&q_empty[s], 1); }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&ds_full[b], 4);
+      mbar_init(&dsm_free[b], 1);
+      mbar_init(&dq_full[b], 1);
+    }
     mbar_init(dq_empty, 4);
-    mbar_init(it_done, 1);
     mbar_init(fin, 1);
     mbar_init(drain, 1);
+    mbar_init(stg, 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -165,99 +185,112 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_it = n_qb * G;   // iteration it -> q head g = it / n_qb, block qb = it % n_qb
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_expect_tx(kv_full, 2 * L::kTileKV);
       for (int c = 0; c < D / 64; ++c) {
         tma_load_3d(sK + c * L::kChunkKV, &tmK, c * 64, (int)k0, kvh, kv_full);
         tma_load_3d(sV + c * L::kChunkKV, &tmV, c * 64, (int)k0, kvh, kv_full);
       }
+      for (int it = 0; it < n_it; ++it) {
+        const int st = it % NSTAGE;
+        const uint32_t round = it / NSTAGE;
+        if (!mbar_wait(&q_empty[st], (round & 1) ^ 1, abort_flag)) break;
+        const int n = kvh * G + it / n_qb;
+        const int q0 = (int)(q_lo + (int64_t)(it % n_qb) * BMQ);
+        mbar_expect_tx(&q_full[st], 2 * L::kTileQ);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(sQ + st * L::kTileQ + c * L::kChunkQ, &tmQ, c * 64, q0, n, &q_full[st]);
+          tma_load_3d(sDO + st * L::kTileQ + c * L::kChunkQ, &tmDO, c * 64, q0, n, &q_full[st]);
+        }
+      }
     }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ LSE / D_i loader
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSTAGE;
       const uint32_t round = it / NSTAGE;
       if (!mbar_wait(&q_empty[st], (round & 1) ^ 1, abort_flag)) break;
       const int n = kvh * G + it / n_qb;
       const int64_t q0 = q_lo + (int64_t)(it % n_qb) * BMQ;
-      // LSE (log2 units) and D_i of the tile's 64 query rows; rows past S get 0
       float* stat = sStat + st * 2 * BMQ;
+#pragma unroll
       for (int r = lane; r < BMQ; r += 32) {
         const int64_t i = q0 + r;
         stat[r] = i < S ? lse[lse_index(n, nq, lse_bstride, S, i)] * kLog2e : 0.f;
         stat[BMQ + r] = i < S ? delta[(int64_t)n * S + i] : 0.f;
       }
       __syncwarp();
-      if (lane == 0) {
-        mbar_expect_tx(&q_full[st], 2 * L::kTileQ);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(sQ + st * L::kTileQ + c * L::kChunkQ, &tmQ, c * 64, (int)q0, n, &q_full[st]);
-          tma_load_3d(sDO + st * L::kTileQ + c * L::kChunkQ, &tmDO, c * 64, (int)q0, n, &q_full[st]);
-        }
-      }
-      __syncwarp();
+      if (lane == 0) mbar_arrive(&q_full[st]);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t id_s = idesc_bf16(BN, BMQ, false, false);    // S^T, dP^T
     constexpr uint32_t id_g = idesc_bf16(BN, D, false, true);       // dV, dK
     constexpr uint32_t id_q = idesc_bf16(D, BMQ, true, true);       // dQ^T
-    const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV), ds_addr = smem_u32(sDS);
-    bool ok = mbar_wait(kv_full, 0, abort_flag);
-    for (int it = 0; ok && it < n_it; ++it) {
+    const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+    auto issue_scores = [&](int it) -> bool {
       const int st = it % NSTAGE;
       const uint32_t round = it / NSTAGE;
-      if (!mbar_wait(&q_full[st], round & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(&q_full[st], round & 1, abort_flag)) return false;
+      // S buffer of this parity held dQ^T_{it-2}: its readout must be done
+      if (it >= 2 && !mbar_wait(dq_empty, (it - 2) & 1, abort_flag)) return false;
       tc_fence_after();
-      const uint32_t q_addr = smem_u32(sQ + st * L::kTileQ);
-      const uint32_t do_addr = smem_u32(sDO + st * L::kTileQ);
       if (lane == 0) {
+        const uint32_t q_addr = smem_u32(sQ + st * L::kTileQ);
+        const uint32_t do_addr = smem_u32(sDO + st * L::kTileQ);
+        const uint32_t b = (uint32_t)(it & 1);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off_kv = (kk >> 2) * L::kChunkKV + (kk & 3) * 32;
           const uint32_t off_q = (kk >> 2) * L::kChunkQ + (kk & 3) * 32;
-          mma_ss(tbase + kColS, sdesc_sw128(k_addr + off_kv, 16, 1024),
+          mma_ss(tbase + kColS + b * BMQ, sdesc_sw128(k_addr + off_kv, 16, 1024),
                  sdesc_sw128(q_addr + off_q, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off_kv = (kk >> 2) * L::kChunkKV + (kk & 3) * 32;
           const uint32_t off_q = (kk >> 2) * L::kChunkQ + (kk & 3) * 32;
-          mma_ss(tbase + kColDP, sdesc_sw128(v_addr + off_kv, 16, 1024),
+          mma_ss(tbase + kColDP + b * BMQ, sdesc_sw128(v_addr + off_kv, 16, 1024),
                  sdesc_sw128(do_addr + off_q, 16, 1024), id_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(s_full);
+        mma_commit(&s_full[b]);
       }
       __syncwarp();
-      if (!mbar_wait(ds_full, it & 1, abort_flag)) { ok = false; break; }
+      return true;
+    };
+    bool ok = mbar_wait(kv_full, 0, abort_flag);
+    if (ok && n_it > 0) ok = issue_scores(0);
+    for (int it = 0; ok && it < n_it; ++it) {
+      if (it + 1 < n_it && !issue_scores(it + 1)) { ok = false; break; }
+      const int st = it % NSTAGE;
+      const uint32_t b = (uint32_t)(it & 1);
+      if (!mbar_wait(&ds_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {
-        // B = dO_i / Q_i as MN-major: 16 queries per step (2048 B), 64-feature
+        const uint32_t q_addr = smem_u32(sQ + st * L::kTileQ);
+        const uint32_t do_addr = smem_u32(sDO + st * L::kTileQ);
+        const uint32_t ds_addr = smem_u32(sDS + b * L::kTileDS);
+        // B = dO_it / Q_it as MN-major: 16 queries per step (2048 B), 64-feature
         // chunks L::kChunkQ apart.
 #pragma unroll
-        for (int kk = 0; kk < BMQ / 16; ++kk) {
-          mma_ts(tbase + kColDV, tbase + kColS + kk * 8, sdesc_sw128(do_addr + kk * 2048, L::kChunkQ, 1024),
-                 id_g, (it > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BMQ / 16; ++kk)
+          mma_ts(tbase + kColDV, tbase + kColS + b * BMQ + kk * 8,
+                 sdesc_sw128(do_addr + kk * 2048, L::kChunkQ, 1024), id_g, (it > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < BMQ / 16; ++kk) {
-          mma_ts(tbase + kColDK, tbase + kColDP + kk * 8, sdesc_sw128(q_addr + kk * 2048, L::kChunkQ, 1024),
-                 id_g, (it > 0 || kk > 0) ? 1u : 0u);
-        }
-      }
-      __syncwarp();
-      if (it > 0 && !mbar_wait(dq_empty, (it - 1) & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {
-        // A = K^T (MN-major: 64-feature chunks L::kChunkKV apart), B = dS^T
-        // ([key][query] rows of 128 B); 16 keys per step.
+        for (int kk = 0; kk < BMQ / 16; ++kk)
+          mma_ts(tbase + kColDK, tbase + kColDP + b * BMQ + kk * 8,
+                 sdesc_sw128(q_addr + kk * 2048, L::kChunkQ, 1024), id_g, (it > 0 || kk > 0) ? 1u : 0u);
+        // dQ^T = K^T dS^T into S buffer b: A = K (MN-major, 64-feature chunks
+        // L::kChunkKV apart), B = dS^T ([key][query] rows of 128 B); 16 keys per step.
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          mma_ss(tbase + kColDQ, sdesc_sw128(k_addr + kk * 2048, L::kChunkKV, 1024),
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ss(tbase + kColS + b * BMQ, sdesc_sw128(k_addr + kk * 2048, L::kChunkKV, 1024),
                  sdesc_sw128(ds_addr + kk * 2048, 8192, 1024), id_q, kk > 0 ? 1u : 0u);
-        }
-        mma_commit(dq_full);
+        mma_commit(&dq_full[b]);
         mma_commit(&q_empty[st]);
-        mma_commit(it_done);
+        mma_commit(&dsm_free[b]);
       }
       __syncwarp();
     }
@@ -267,62 +300,108 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     mbar_wait(drain, 0, nullptr);
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ gradient warps
+    // Thread = key row jr for P^T/dS^T (TMEM lane), and = feature d for the
+    // dQ^T readout (also TMEM lane wq*32 + lane).
     const int wq = warp & 3;
-    const int jr = wq * 32 + lane;               // key row in the block = TMEM lane
+    const int jr = wq * 32 + lane;
     const int64_t j = k0 + jr;
     int64_t qlo = 0, qhi = 0;
     if (j < S) query_range(cu, nd, S, causal, j, qlo, qhi);
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float sl2 = scale * kLog2e;
+    float* sDQ = reinterpret_cast<float*>(smem + L::kDQ);
+    const bool leader = (warp == 4 && lane == 0);
     bool ok = true;
+    uint32_t n_sync = 0;
+    // bounded sync of the four gradient warps (an mbarrier phase per call)
+    auto group_sync = [&]() -> bool {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(stg);
+      return mbar_wait(stg, (n_sync++) & 1, abort_flag);
+    };
+
+    // dQ^T of tile x (in S buffer x & 1) -> shared staging -> one bulk
+    // reduce-add of the tile's rows into dQ.
+    auto readout = [&](int x) -> bool {
+      const uint32_t bx = (uint32_t)(x & 1);
+      if (!mbar_wait(&dq_full[bx], (x >> 1) & 1, abort_flag)) return false;
+      tc_fence_after();
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tbase + lane_off + kColS + bx * BMQ, r0);
+      tmem_ld32(tbase + lane_off + kColS + bx * BMQ + 32, r1);
+      tmem_ld_wait();
+      reg_fence(r0);
+      reg_fence(r1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_empty);
+      if (leader) bulk_wait_read0();          // previous tile's reduce has read the staging
+      if (!group_sync()) return false;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) sDQ[c * D + jr] = __uint_as_float(r0[c]) * scale;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) sDQ[(32 + c) * D + jr] = __uint_as_float(r1[c]) * scale;
+      fence_async_smem();
+      if (!group_sync()) return false;
+      if (leader) {
+        const int n = kvh * G + x / n_qb;
+        const int64_t q0 = q_lo + (int64_t)(x % n_qb) * BMQ;
+        const int64_t rows = S - q0 < BMQ ? S - q0 : BMQ;
+        if (rows > 0) {
+          bulk_reduce_add_f32(dq + ((int64_t)n * S + q0) * D, sDQ, (uint32_t)(rows * D * 4));
+          bulk_commit();
+        }
+      }
+      return true;
+    };
+
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSTAGE;
       const uint32_t round = it / NSTAGE;
+      const uint32_t b = (uint32_t)(it & 1);
       const int64_t q0 = q_lo + (int64_t)(it % n_qb) * BMQ;
       if (!mbar_wait(&q_full[st], round & 1, abort_flag)) { ok = false; break; }
-      if (!mbar_wait(s_full, it & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(&s_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const float* stat = sStat + st * 2 * BMQ;
       const bool full = (q0 >= qlo) && (q0 + BMQ <= qhi);
+      uint32_t sv[2][32], pv[2][32];
+      tmem_ld32(tbase + lane_off + kColS + b * BMQ, sv[0]);
+      tmem_ld32(tbase + lane_off + kColS + b * BMQ + 32, sv[1]);
+      tmem_ld32(tbase + lane_off + kColDP + b * BMQ, pv[0]);
+      tmem_ld32(tbase + lane_off + kColDP + b * BMQ + 32, pv[1]);
+      tmem_ld_wait();
+      reg_fence(sv[0]); reg_fence(sv[1]); reg_fence(pv[0]); reg_fence(pv[1]);
       uint32_t pp[32], dd[32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t sv[32], pv[32];
-        tmem_ld32(tbase + lane_off + kColS + c * 32, sv);
-        tmem_ld32(tbase + lane_off + kColDP + c * 32, pv);
-        tmem_ld_wait();
-        reg_fence(sv);
-        reg_fence(pv);
+      for (int col = 0; col < BMQ; col += 4) {
+        const int c = col >> 5, e4 = col & 31;
+        const float4 l4 = *reinterpret_cast<const float4*>(stat + col);
+        const float4 d4 = *reinterpret_cast<const float4*>(stat + BMQ + col);
+        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+        const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+        float p[4], g[4];
 #pragma unroll
-        for (int e4 = 0; e4 < 32; e4 += 4) {
-          const int col = c * 32 + e4;
-          const float4 l4 = *reinterpret_cast<const float4*>(stat + col);
-          const float4 d4 = *reinterpret_cast<const float4*>(stat + BMQ + col);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-          float p[4], g[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            p[u] = ex2(fmaf(__uint_as_float(sv[e4 + u]), sl2, -lv[u]));
-            if (!full) {
-              const int64_t i = q0 + col + u;
-              p[u] = (i >= qlo && i < qhi) ? p[u] : 0.f;
-            }
-            g[u] = p[u] * (__uint_as_float(pv[e4 + u]) - dl[u]);
+        for (int u = 0; u < 4; ++u) {
+          p[u] = ex2(fmaf(__uint_as_float(sv[c][e4 + u]), sl2, -lv[u]));
+          if (!full) {
+            const int64_t i = q0 + col + u;
+            p[u] = (i >= qlo && i < qhi) ? p[u] : 0.f;
           }
-          pp[col >> 1] = pack_bf16(p[0], p[1]);
-          pp[(col >> 1) + 1] = pack_bf16(p[2], p[3]);
-          dd[col >> 1] = pack_bf16(g[0], g[1]);
-          dd[(col >> 1) + 1] = pack_bf16(g[2], g[3]);
+          g[u] = p[u] * (__uint_as_float(pv[c][e4 + u]) - dl[u]);
         }
+        pp[col >> 1] = pack_bf16(p[0], p[1]);
+        pp[(col >> 1) + 1] = pack_bf16(p[2], p[3]);
+        dd[col >> 1] = pack_bf16(g[0], g[1]);
+        dd[(col >> 1) + 1] = pack_bf16(g[2], g[3]);
       }
-      tmem_st32(tbase + lane_off + kColS, pp);
-      tmem_st32(tbase + lane_off + kColDP, dd);
-      // the previous iteration's dQ^T MMA must be done reading dS^T
-      if (it > 0 && !mbar_wait(it_done, (it - 1) & 1, abort_flag)) { ok = false; break; }
-      uint8_t* row = sDS + jr * 128;
+      tmem_st32(tbase + lane_off + kColS + b * BMQ, pp);
+      tmem_st32(tbase + lane_off + kColDP + b * BMQ, dd);
+      // dS^T smem buffer b was last read by dQ^T_{it-2}
+      if (it >= 2 && !mbar_wait(&dsm_free[b], ((it - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
+      uint8_t* row = sDS + b * L::kTileDS + jr * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint4 w = make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]);
@@ -332,8 +411,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(ds_full);
+      if (lane == 0) mbar_arrive(&ds_full[b]);
+      // the previous tile's dQ^T is (or soon will be) ready: flush it
+      if (it >= 1 && !readout(it - 1)) { ok = false; break; }
     }
+    if (ok && n_it > 0 && !readout(n_it - 1)) ok = false;
     // epilogue: dV and scale * dK of this key block
     if (ok && n_it > 0 && mbar_wait(fin, 0, abort_flag)) {
       tc_fence_after();
@@ -364,34 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float4*>(dk + ((int64_t)kvh * S + j) * D + c) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     }
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ dQ readout
-    const int wq = warp & 3;
-    const int d = wq * 32 + lane;                // feature = TMEM lane of dQ^T
-    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
-    for (int it = 0; it < n_it; ++it) {
-      if (!mbar_wait(dq_full, it & 1, abort_flag)) break;
-      tc_fence_after();
-      uint32_t r[2][32];
-      tmem_ld32(tbase + lane_off + kColDQ, r[0]);
-      tmem_ld32(tbase + lane_off + kColDQ + 32, r[1]);
-      tmem_ld_wait();
-      reg_fence(r[0]);
-      reg_fence(r[1]);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_empty);
-      const int n = kvh * G + it / n_qb;
-      const int64_t q0 = q_lo + (int64_t)(it % n_qb) * BMQ;
-      float* base = dq + ((int64_t)n * S + q0) * D + d;
-#pragma unroll
-      for (int c = 0; c < 2; ++c)
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int col = c * 32 + e;
-          if (q0 + col < S) atomicAdd(base + (int64_t)col * D, __uint_as_float(r[c][e]) * scale);
-        }
-    }
+    if (leader) bulk_wait0();   // every dQ reduce has landed before the CTA retires
   }
 
   tc_fence_before();
