@@ -23,13 +23,15 @@
 //   dK  += dS^T Q_i            (A = dS^T from TMEM, B = Q_i, MN-major)
 //   dQ_i^T = K^T dS^T          (M = D, N = 64 queries; A = K, MN-major;
 //                               B = dS^T from shared memory, MN-major)
-// The gradient warps then read dQ_i^T out of TMEM (lane = feature d), stage
-// scale * dQ_i in shared memory as [query][feature] rows and add the tile's
-// rows into the fp32 dQ with one TMA bulk reduce-add (cp.reduce.async.bulk).
+// The gradient warps then read dQ_i^T out of TMEM (lane = feature d) and
+// write scale * dQ_i as [query][feature] fp32 rows into the tile's consumed
+// Q/dO stage buffers; a flusher warp adds them into dQ with TMA bulk
+// reduce-adds (cp.reduce.async.bulk) and then releases the stage.
 //
-// Warp roles (256 threads): 0 TMA producer, 1 TMEM owner and MMA issuer,
-// 2 LSE/D_i loader, 4-7 softmax/gradient warps (thread = key row for P/dS,
-// feature for the dQ readout).  TMEM columns: dV [0,128), dK [128,256), two
+// Warp roles (384 threads): 0 TMA producer, 1 TMEM owner and MMA issuer,
+// 2 LSE/D_i loader, 3 dQ flusher, 4-11 gradient warps: two per TMEM lane
+// quarter, each taking 32 of the tile's 64 queries (thread = key row for
+// P/dS, feature for the dQ readout).  TMEM columns: dV [0,128), dK [128,256), two
 // S^T/P^T buffers [256,384) that also receive each tile's dQ^T, two
 // dP^T/dS^T buffers [384,512).
 #include "internal.h"
@@ -46,8 +48,9 @@ using namespace tc;
 constexpr int BN = 128;     // keys per CTA
 constexpr int BMQ = 64;     // queries per inner tile
 constexpr int D = 128;
-constexpr int NSTAGE = 2;   // Q/dO/LSE/D_i ring
-constexpr int kThreads = 256;
+constexpr int NSTAGE = 4;   // Q/dO/LSE/D_i ring (a consumed stage also stages its dQ tile)
+constexpr int kThreads = 384;
+constexpr int kGradWarps = 8;   // warps 4..11: two per TMEM lane quarter, one per 32-query half
 constexpr uint32_t kTmemCols = 512;
 // TMEM: dV, dK accumulators; two S^T/P^T buffers (each later reused for the
 // tile's dQ^T); two dP^T/dS^T buffers.
@@ -64,13 +67,12 @@ struct BwdLayout {
   static constexpr int kV = kK + kTileKV;
   static constexpr int kQ = kV + kTileKV;                    // NSTAGE tiles
   static constexpr int kDO = kQ + NSTAGE * kTileQ;            // NSTAGE tiles
-  static constexpr int kDS = kDO + NSTAGE * kTileQ;           // 2 tiles
-  static constexpr int kDQ = kDS + 2 * kTileDS;               // dQ tile staging [64 q][128 d] fp32
-  static constexpr int kStat = kDQ + BMQ * D * 4;             // NSTAGE x {LSE2[64], D[64]}
+  static constexpr int kDS = kDO + NSTAGE * kTileQ;           // one dS^T tile
+  static constexpr int kStat = kDS + kTileDS;                 // NSTAGE x {LSE2[64], D[64]}
   static constexpr int kBar = kStat + NSTAGE * 2 * BMQ * 4;
-  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[2], ds_full[2], dsm_free[2],
-  // dq_full[2], dq_empty, fin, drain, stg (gradient-warp group sync)
-  static constexpr int kNumBar = 1 + 2 * NSTAGE + 8 + 4;
+  // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[2], ds_full[2], dsm_free,
+  // dq_full[2], dq_empty, fin, drain, stg_full[NSTAGE]
+  static constexpr int kNumBar = 1 + 3 * NSTAGE + 7 + 3;
   static constexpr int kMisc = kBar + kNumBar * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 //                                                   lived in S buffer b')
 //   wait ds_full[b]  (gradient warps finished tile it)
 //   dV += P^T_it dO_it, dK += dS^T_it Q_it, dQ^T_it = K^T dS^T_it  (into S buffer b)
-//   -> dq_full[b], q_empty[stage], dsm_free[b]
+//   -> dq_full[b], dsm_free
 // so the tensor pipe runs tile it's gradient MMAs and tile it+1's score MMAs
 // while the gradient warps work on tile it+1.
 __global__ void __launch_bounds__(kThreads, 1)
@@ -134,11 +136,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = q_empty + NSTAGE;
   uint64_t* ds_full = s_full + 2;
   uint64_t* dsm_free = ds_full + 2;
-  uint64_t* dq_full = dsm_free + 2;
+  uint64_t* dq_full = dsm_free + 1;
   uint64_t* dq_empty = dq_full + 2;
   uint64_t* fin = dq_empty + 1;
   uint64_t* drain = fin + 1;
-  uint64_t* stg = drain + 1;
+  uint64_t* stg_full = drain + 1;     // dQ tile of a stage written to its Q/dO buffers
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -148,17 +150,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int s = 0; s < NSTAGE; ++s) { mbar_init(&q_full[s], 2); mbar_init(&q_empty[s], 1); }
+    for (int s = 0; s < NSTAGE; ++s) {
+      mbar_init(&q_full[s], 2);
+      mbar_init(&q_empty[s], 1);
+      mbar_init(&stg_full[s], kGradWarps);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&ds_full[b], 4);
-      mbar_init(&dsm_free[b], 1);
+      mbar_init(&ds_full[b], kGradWarps);
       mbar_init(&dq_full[b], 1);
     }
-    mbar_init(dq_empty, 4);
+    mbar_init(dq_empty, kGradWarps);
+    mbar_init(dsm_free, 1);
     mbar_init(fin, 1);
     mbar_init(drain, 1);
-    mbar_init(stg, 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -230,6 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t id_g = idesc_bf16(BN, D, false, true);       // dV, dK
     constexpr uint32_t id_q = idesc_bf16(D, BMQ, true, true);       // dQ^T
     const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+    const uint64_t kd_k = sdesc_sw128(k_addr, 16, 1024);           // K, K-major
+    const uint64_t vd_k = sdesc_sw128(v_addr, 16, 1024);           // V, K-major
+    const uint64_t kd_mn = sdesc_sw128(k_addr, L::kChunkKV, 1024);  // K^T, MN-major
     auto issue_scores = [&](int it) -> bool {
       const int st = it % NSTAGE;
       const uint32_t round = it / NSTAGE;
@@ -238,22 +246,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it >= 2 && !mbar_wait(dq_empty, (it - 2) & 1, abort_flag)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t q_addr = smem_u32(sQ + st * L::kTileQ);
-        const uint32_t do_addr = smem_u32(sDO + st * L::kTileQ);
+        const uint64_t qd = sdesc_sw128(smem_u32(sQ + st * L::kTileQ), 16, 1024);
+        const uint64_t dod = sdesc_sw128(smem_u32(sDO + st * L::kTileQ), 16, 1024);
         const uint32_t b = (uint32_t)(it & 1);
+        // S^T and dP^T are independent accumulators: interleave them per K step
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off_kv = (kk >> 2) * L::kChunkKV + (kk & 3) * 32;
           const uint32_t off_q = (kk >> 2) * L::kChunkQ + (kk & 3) * 32;
-          mma_ss(tbase + kColS + b * BMQ, sdesc_sw128(k_addr + off_kv, 16, 1024),
-                 sdesc_sw128(q_addr + off_q, 16, 1024), id_s, kk > 0 ? 1u : 0u);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off_kv = (kk >> 2) * L::kChunkKV + (kk & 3) * 32;
-          const uint32_t off_q = (kk >> 2) * L::kChunkQ + (kk & 3) * 32;
-          mma_ss(tbase + kColDP + b * BMQ, sdesc_sw128(v_addr + off_kv, 16, 1024),
-                 sdesc_sw128(do_addr + off_q, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          mma_ss(tbase + kColS + b * BMQ, sdesc_add(kd_k, off_kv), sdesc_add(qd, off_q), id_s, kk > 0 ? 1u : 0u);
+          mma_ss(tbase + kColDP + b * BMQ, sdesc_add(vd_k, off_kv), sdesc_add(dod, off_q), id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[b]);
       }
@@ -269,28 +271,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&ds_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t q_addr = smem_u32(sQ + st * L::kTileQ);
-        const uint32_t do_addr = smem_u32(sDO + st * L::kTileQ);
-        const uint32_t ds_addr = smem_u32(sDS + b * L::kTileDS);
         // B = dO_it / Q_it as MN-major: 16 queries per step (2048 B), 64-feature
         // chunks L::kChunkQ apart.
+        const uint64_t dod = sdesc_sw128(smem_u32(sDO + st * L::kTileQ), L::kChunkQ, 1024);
+        const uint64_t qd = sdesc_sw128(smem_u32(sQ + st * L::kTileQ), L::kChunkQ, 1024);
+        const uint64_t dsd = sdesc_sw128(smem_u32(sDS), 8192, 1024);
+        // dV and dK are independent: interleave per K step
 #pragma unroll
-        for (int kk = 0; kk < BMQ / 16; ++kk)
-          mma_ts(tbase + kColDV, tbase + kColS + b * BMQ + kk * 8,
-                 sdesc_sw128(do_addr + kk * 2048, L::kChunkQ, 1024), id_g, (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < BMQ / 16; ++kk)
-          mma_ts(tbase + kColDK, tbase + kColDP + b * BMQ + kk * 8,
-                 sdesc_sw128(q_addr + kk * 2048, L::kChunkQ, 1024), id_g, (it > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < BMQ / 16; ++kk) {
+          mma_ts(tbase + kColDV, tbase + kColS + b * BMQ + kk * 8, sdesc_add(dod, kk * 2048), id_g,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tbase + kColDK, tbase + kColDP + b * BMQ + kk * 8, sdesc_add(qd, kk * 2048), id_g,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        }
         // dQ^T = K^T dS^T into S buffer b: A = K (MN-major, 64-feature chunks
         // L::kChunkKV apart), B = dS^T ([key][query] rows of 128 B); 16 keys per step.
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ss(tbase + kColS + b * BMQ, sdesc_sw128(k_addr + kk * 2048, L::kChunkKV, 1024),
-                 sdesc_sw128(ds_addr + kk * 2048, 8192, 1024), id_q, kk > 0 ? 1u : 0u);
+          mma_ss(tbase + kColS + b * BMQ, sdesc_add(kd_mn, kk * 2048), sdesc_add(dsd, kk * 2048), id_q,
+                 kk > 0 ? 1u : 0u);
         mma_commit(&dq_full[b]);
-        mma_commit(&q_empty[st]);
-        mma_commit(&dsm_free[b]);
+        mma_commit(dsm_free);
       }
       __syncwarp();
     }
@@ -300,60 +301,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
     mbar_wait(drain, 0, nullptr);
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ dQ flusher
+    // Tile x's dQ rows sit in its (consumed) Q buffer (rows 0-31) and dO
+    // buffer (rows 32-63); add them into dQ with bulk reductions, then hand
+    // the stage back to the producer once the reads are done.
+    if (lane == 0) {
+      for (int x = 0; x < n_it; ++x) {
+        const int st = x % NSTAGE;
+        if (!mbar_wait(&stg_full[st], (x / NSTAGE) & 1, abort_flag)) break;
+        const int n = kvh * G + x / n_qb;
+        const int64_t q0 = q_lo + (int64_t)(x % n_qb) * BMQ;
+        const int64_t rows = S - q0 < BMQ ? S - q0 : BMQ;
+        float* dst = dq + ((int64_t)n * S + q0) * D;
+        const int64_t r0 = rows < 32 ? rows : 32;
+        if (r0 > 0) bulk_reduce_add_f32(dst, sQ + st * L::kTileQ, (uint32_t)(r0 * D * 4));
+        if (rows > 32) bulk_reduce_add_f32(dst + 32 * D, sDO + st * L::kTileQ, (uint32_t)((rows - 32) * D * 4));
+        bulk_commit();
+        bulk_wait_read0();
+        mbar_arrive(&q_empty[st]);
+      }
+      bulk_wait0();   // every dQ reduce has landed before the CTA retires
+    }
+    __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ gradient warps
-    // Thread = key row jr for P^T/dS^T (TMEM lane), and = feature d for the
-    // dQ^T readout (also TMEM lane wq*32 + lane).
+    // Warp (4 + 4h + wq): TMEM lane quarter wq, query half h (columns
+    // [32h, 32h+32) of the 64-query tile).  Thread = key row jr for P^T/dS^T,
+    // and = feature d for the dQ^T readout (both TMEM lane wq*32 + lane).
     const int wq = warp & 3;
+    const int h = (warp - 4) >> 2;
     const int jr = wq * 32 + lane;
     const int64_t j = k0 + jr;
     int64_t qlo = 0, qhi = 0;
     if (j < S) query_range(cu, nd, S, causal, j, qlo, qhi);
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const float sl2 = scale * kLog2e;
-    float* sDQ = reinterpret_cast<float*>(smem + L::kDQ);
-    const bool leader = (warp == 4 && lane == 0);
     bool ok = true;
-    uint32_t n_sync = 0;
-    // bounded sync of the four gradient warps (an mbarrier phase per call)
-    auto group_sync = [&]() -> bool {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(stg);
-      return mbar_wait(stg, (n_sync++) & 1, abort_flag);
-    };
 
-    // dQ^T of tile x (in S buffer x & 1) -> shared staging -> one bulk
-    // reduce-add of the tile's rows into dQ.
+    // dQ^T of tile x (in S buffer x & 1) -> scale * dQ rows [32h, 32h+32) of
+    // the tile written as [query][feature] fp32 rows into tile x's consumed
+    // Q (h = 0) or dO (h = 1) buffer; the flusher warp adds them into dQ.
     auto readout = [&](int x) -> bool {
       const uint32_t bx = (uint32_t)(x & 1);
+      const int sx = x % NSTAGE;
       if (!mbar_wait(&dq_full[bx], (x >> 1) & 1, abort_flag)) return false;
       tc_fence_after();
-      uint32_t r0[32], r1[32];
-      tmem_ld32(tbase + lane_off + kColS + bx * BMQ, r0);
-      tmem_ld32(tbase + lane_off + kColS + bx * BMQ + 32, r1);
+      uint32_t r[32];
+      tmem_ld32(tbase + lane_off + kColS + bx * BMQ + h * 32, r);
       tmem_ld_wait();
-      reg_fence(r0);
-      reg_fence(r1);
+      reg_fence(r);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dq_empty);
-      if (leader) bulk_wait_read0();          // previous tile's reduce has read the staging
-      if (!group_sync()) return false;
+      float* col = reinterpret_cast<float*>((h == 0 ? sQ : sDO) + sx * L::kTileQ) + jr;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) sDQ[c * D + jr] = __uint_as_float(r0[c]) * scale;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) sDQ[(32 + c) * D + jr] = __uint_as_float(r1[c]) * scale;
+      for (int c = 0; c < 32; ++c) col[c * D] = __uint_as_float(r[c]) * scale;
       fence_async_smem();
-      if (!group_sync()) return false;
-      if (leader) {
-        const int n = kvh * G + x / n_qb;
-        const int64_t q0 = q_lo + (int64_t)(x % n_qb) * BMQ;
-        const int64_t rows = S - q0 < BMQ ? S - q0 : BMQ;
-        if (rows > 0) {
-          bulk_reduce_add_f32(dq + ((int64_t)n * S + q0) * D, sDQ, (uint32_t)(rows * D * 4));
-          bulk_commit();
-        }
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&stg_full[sx]);
       return true;
     };
 
@@ -361,23 +367,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int st = it % NSTAGE;
       const uint32_t round = it / NSTAGE;
       const uint32_t b = (uint32_t)(it & 1);
-      const int64_t q0 = q_lo + (int64_t)(it % n_qb) * BMQ;
+      const int64_t q0 = q_lo + (int64_t)(it % n_qb) * BMQ + h * 32;   // this half's first query
       if (!mbar_wait(&q_full[st], round & 1, abort_flag)) { ok = false; break; }
       if (!mbar_wait(&s_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      const float* stat = sStat + st * 2 * BMQ;
-      const bool full = (q0 >= qlo) && (q0 + BMQ <= qhi);
-      uint32_t sv[2][32], pv[2][32];
-      tmem_ld32(tbase + lane_off + kColS + b * BMQ, sv[0]);
-      tmem_ld32(tbase + lane_off + kColS + b * BMQ + 32, sv[1]);
-      tmem_ld32(tbase + lane_off + kColDP + b * BMQ, pv[0]);
-      tmem_ld32(tbase + lane_off + kColDP + b * BMQ + 32, pv[1]);
+      const float* stat = sStat + st * 2 * BMQ + h * 32;
+      const bool full = (q0 >= qlo) && (q0 + 32 <= qhi);
+      uint32_t sv[32], pv[32];
+      tmem_ld32(tbase + lane_off + kColS + b * BMQ + h * 32, sv);
+      tmem_ld32(tbase + lane_off + kColDP + b * BMQ + h * 32, pv);
       tmem_ld_wait();
-      reg_fence(sv[0]); reg_fence(sv[1]); reg_fence(pv[0]); reg_fence(pv[1]);
-      uint32_t pp[32], dd[32];
+      reg_fence(sv);
+      reg_fence(pv);
+      uint32_t pp[16], dd[16];
 #pragma unroll
-      for (int col = 0; col < BMQ; col += 4) {
-        const int c = col >> 5, e4 = col & 31;
+      for (int col = 0; col < 32; col += 4) {
         const float4 l4 = *reinterpret_cast<const float4*>(stat + col);
         const float4 d4 = *reinterpret_cast<const float4*>(stat + BMQ + col);
         const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
@@ -385,27 +389,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         float p[4], g[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          p[u] = ex2(fmaf(__uint_as_float(sv[c][e4 + u]), sl2, -lv[u]));
+          p[u] = ex2(fmaf(__uint_as_float(sv[col + u]), sl2, -lv[u]));
           if (!full) {
             const int64_t i = q0 + col + u;
             p[u] = (i >= qlo && i < qhi) ? p[u] : 0.f;
           }
-          g[u] = p[u] * (__uint_as_float(pv[c][e4 + u]) - dl[u]);
+          g[u] = p[u] * (__uint_as_float(pv[col + u]) - dl[u]);
         }
         pp[col >> 1] = pack_bf16(p[0], p[1]);
         pp[(col >> 1) + 1] = pack_bf16(p[2], p[3]);
         dd[col >> 1] = pack_bf16(g[0], g[1]);
         dd[(col >> 1) + 1] = pack_bf16(g[2], g[3]);
       }
-      tmem_st32(tbase + lane_off + kColS + b * BMQ, pp);
-      tmem_st32(tbase + lane_off + kColDP + b * BMQ, dd);
-      // dS^T smem buffer b was last read by dQ^T_{it-2}
-      if (it >= 2 && !mbar_wait(&dsm_free[b], ((it - 2) >> 1) & 1, abort_flag)) { ok = false; break; }
-      uint8_t* row = sDS + b * L::kTileDS + jr * 128;
+      // bf16 pairs: 16 columns per half
+      tmem_st16(tbase + lane_off + kColS + b * BMQ + h * 16, pp);
+      tmem_st16(tbase + lane_off + kColDP + b * BMQ + h * 16, dd);
+      // the dS^T tile in shared memory was last read by dQ^T_{it-1}
+      if (it >= 1 && !mbar_wait(dsm_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
+      uint8_t* row = sDS + jr * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
+        const int lc = h * 4 + c;                 // logical 16-byte chunk of the 128-byte row
         uint4 w = make_uint4(dd[4 * c], dd[4 * c + 1], dd[4 * c + 2], dd[4 * c + 3]);
-        *reinterpret_cast<uint4*>(row + ((c ^ (jr & 7)) << 4)) = w;
+        *reinterpret_cast<uint4*>(row + ((lc ^ (jr & 7)) << 4)) = w;
       }
       fence_async_smem();
       tmem_st_wait();
@@ -416,37 +422,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it >= 1 && !readout(it - 1)) { ok = false; break; }
     }
     if (ok && n_it > 0 && !readout(n_it - 1)) ok = false;
-    // epilogue: dV and scale * dK of this key block
+    // epilogue: half 0 writes dV, half 1 writes scale * dK of this key block
     if (ok && n_it > 0 && mbar_wait(fin, 0, abort_flag)) {
       tc_fence_after();
+      float* dst = (h == 0 ? dv : dk) + ((int64_t)kvh * S + j) * D;
+      const float mul = h == 0 ? 1.f : scale;
+      const uint32_t col0 = h == 0 ? kColDV : kColDK;
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        float* dst = (which == 0 ? dv : dk) + ((int64_t)kvh * S + j) * D;
-        const float mul = which == 0 ? 1.f : scale;
-        const uint32_t col0 = which == 0 ? kColDV : kColDK;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tbase + lane_off + col0 + c * 32, r);
-          tmem_ld_wait();
-          reg_fence(r);
-          if (j < S) {
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tbase + lane_off + col0 + c * 32, r);
+        tmem_ld_wait();
+        reg_fence(r);
+        if (j < S) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4)
-              *reinterpret_cast<float4*>(dst + c * 32 + e) =
-                  make_float4(__uint_as_float(r[e]) * mul, __uint_as_float(r[e + 1]) * mul,
-                              __uint_as_float(r[e + 2]) * mul, __uint_as_float(r[e + 3]) * mul);
-          }
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + c * 32 + e) =
+                make_float4(__uint_as_float(r[e]) * mul, __uint_as_float(r[e + 1]) * mul,
+                            __uint_as_float(r[e + 2]) * mul, __uint_as_float(r[e + 3]) * mul);
         }
       }
     } else if (n_it == 0 && j < S) {
       // no query sees these keys: zero gradients
-      for (int c = 0; c < D; c += 4) {
-        *reinterpret_cast<float4*>(dv + ((int64_t)kvh * S + j) * D + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(dk + ((int64_t)kvh * S + j) * D + c) = make_float4(0.f, 0.f, 0.f, 0.f);
-      }
+      float* dst = (h == 0 ? dv : dk) + ((int64_t)kvh * S + j) * D;
+      for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (leader) bulk_wait0();   // every dQ reduce has landed before the CTA retires
   }
 
   tc_fence_before();

@@ -148,20 +148,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t q_addr = smem_u32(sQ);
     bool ok = mbar_wait(q_full, 0, abort_flag);
 
+    const uint64_t qdesc = sdesc_sw128(q_addr, 16, 1024);
     auto issue_qk = [&](int j) -> bool {
       const int idx = 2 * j, slot = idx % NSLOT;
       const uint32_t round = idx / NSLOT;
       if (!mbar_wait(&kv_full[slot], round & 1, abort_flag)) return false;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t k_addr = smem_u32(sKV + slot * L::kTileKV);
+        const uint64_t kdesc = sdesc_sw128(smem_u32(sKV + slot * L::kTileKV), 16, 1024);
         const uint32_t d_tmem = tbase + (uint32_t)(j & 1) * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * 0 + (kk & 3) * 32;
-          const uint64_t a = sdesc_sw128(q_addr + (kk >> 2) * L::kChunkQ + koff, 16, 1024);
-          const uint64_t b = sdesc_sw128(k_addr + (kk >> 2) * L::kChunkKV + koff, 16, 1024);
-          mma_ss(d_tmem, a, b, idesc_qk, kk > 0 ? 1u : 0u);
+          // K-major: 16 features = 32 bytes along the swizzled row, 64-feature chunks apart
+          const uint32_t off = (kk >> 2) * L::kChunkQ + (kk & 3) * 32;
+          const uint32_t offk = (kk >> 2) * L::kChunkKV + (kk & 3) * 32;
+          mma_ss(d_tmem, sdesc_add(qdesc, off), sdesc_add(kdesc, offk), idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[j & 1]);
         mma_commit(&kv_empty[slot]);
@@ -179,15 +180,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(&kv_full[slot], round & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t v_addr = smem_u32(sKV + slot * L::kTileKV);
+        // V as the MN-major B operand: 16 keys = two 8-row groups (1024 B apart),
+        // 64-wide D chunks L::kChunkKV apart.
+        const uint64_t vdesc = sdesc_sw128(smem_u32(sKV + slot * L::kTileKV), L::kChunkKV, 1024);
         const uint32_t p_tmem = tbase + (uint32_t)(j & 1) * BN;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // V as the MN-major B operand: 16 keys = two 8-row groups (1024 B apart),
-          // 64-wide D chunks L::kChunkKV apart.
-          const uint64_t b = sdesc_sw128(v_addr + kk * 2048, L::kChunkKV, 1024);
-          mma_ts(tbase + 256, p_tmem + kk * 8, b, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ts(tbase + 256, p_tmem + kk * 8, sdesc_add(vdesc, kk * 2048), idesc_pv,
+                 (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit(o_done);
         mma_commit(&kv_empty[slot]);
       }
