@@ -57,6 +57,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// TMEM column of bf16 K-step kk (16 queries) of a packed P^T / dS^T tile: each
+// 32-query half is packed into the first 16 columns of its own 32 fp32
+// columns, so neither half overwrites scores the other half still reads.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return (uint32_t)((kk >> 1) * 32 + (kk & 1) * 8); }
+
 struct BwdLayout {
   static constexpr int kChunkKV = BN * 128;          // 64 features x 128 keys
   static constexpr int kChunkQ = BMQ * 128;          // 64 features x 64 queries
@@ -279,9 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dV and dK are independent: interleave per K step
 #pragma unroll
         for (int kk = 0; kk < BMQ / 16; ++kk) {
-          mma_ts(tbase + kColDV, tbase + kColS + b * BMQ + kk * 8, sdesc_add(dod, kk * 2048), id_g,
+          mma_ts(tbase + kColDV, tbase + kColS + b * BMQ + packed_col(kk), sdesc_add(dod, kk * 2048), id_g,
                  (it > 0 || kk > 0) ? 1u : 0u);
-          mma_ts(tbase + kColDK, tbase + kColDP + b * BMQ + kk * 8, sdesc_add(qd, kk * 2048), id_g,
+          mma_ts(tbase + kColDK, tbase + kColDP + b * BMQ + packed_col(kk), sdesc_add(qd, kk * 2048), id_g,
                  (it > 0 || kk > 0) ? 1u : 0u);
         }
         // dQ^T = K^T dS^T into S buffer b: A = K (MN-major, 64-feature chunks
@@ -401,9 +406,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         dd[col >> 1] = pack_bf16(g[0], g[1]);
         dd[(col >> 1) + 1] = pack_bf16(g[2], g[3]);
       }
-      // bf16 pairs: 16 columns per half
-      tmem_st16(tbase + lane_off + kColS + b * BMQ + h * 16, pp);
-      tmem_st16(tbase + lane_off + kColDP + b * BMQ + h * 16, dd);
+      // bf16 pairs: 16 columns per half, inside the half's own 32 columns
+      tmem_st16(tbase + lane_off + kColS + b * BMQ + h * 32, pp);
+      tmem_st16(tbase + lane_off + kColDP + b * BMQ + h * 32, dd);
       // the dS^T tile in shared memory was last read by dQ^T_{it-1}
       if (it >= 1 && !mbar_wait(dsm_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
       uint8_t* row = sDS + jr * 128;
