@@ -129,6 +129,31 @@ int ulysses_attn_bwd(const void* q_h, const void* k_h, const void* v_h, const vo
                      int causal, float scale, int dtype, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * ulysses_attn_bwd without a workspace argument (no counterpart in the pages:
+ * this is an interface convenience).  For callers that cannot allocate device
+ * memory themselves: plugins running inside a host framework that owns every
+ * device allocation, loops where a cudaMalloc (which may synchronise the
+ * device) is not acceptable, or processes under a hard memory cap.
+ *   Arguments, layouts, outputs and errors are those of ulysses_attn_bwd; the
+ *   D_i scratch comes from a 16 MiB array built into the library (every GPU
+ *   that loads the library holds it until the process exits).
+ *   Limit: B * (heads in the stage) * S <= 4,194,304 rows; larger shapes are
+ *   rejected with ULYSSES_ERR_UNSUPPORTED (use ulysses_attn_bwd).
+ *   The library itself allocates nothing here (no cudaMalloc/cudaFree).
+ *   The first call on a device looks up the array's device address with that
+ *   device current; make that first call before any stream capture.
+ *   All calls share the one array: calls that overlap on the GPU (different
+ *   streams, or host threads without ordering) race on it and must be
+ *   serialised by the caller.  The array keeps the last call's D_i values;
+ *   every call rewrites the rows it uses before reading them.
+ * ------------------------------------------------------------------------- */
+int ulysses_attn_bwd_noalloc(const void* q_h, const void* k_h, const void* v_h, const void* o_h,
+                             const void* do_h, const float* lse, float* dq_h, float* dk_h, float* dv_h,
+                             int64_t S, int B, int H_q, int H_kv, int D, int P, int head_chunk,
+                             int stage, const int32_t* cu_seqlens, int num_docs, int causal,
+                             float scale, int dtype, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Whole layer (steps 3-5, forward or backward) with the UPipe stage loop run
  * natively: for every rank r and chunk c, seq2head of the stage's Q/K/V
  * (and O/dO), attention, head2seq of the results.  Head-layout buffers of one

@@ -8,6 +8,7 @@
 // commentary).  UPipe chunks must hold whole kv heads under GQA.
 #include <atomic>
 #include <cstdarg>
+#include <mutex>
 #include <cstdio>
 #include <cstring>
 
@@ -178,6 +179,36 @@ LayerWs layer_ws(char* base, int64_t S, int B, int Cq, int Ckv, int D, int elt) 
   return w;
 }
 
+// ---------------------------------------------------------------------------
+// Scratch for ulysses_attn_bwd_noalloc: the backward's per-row D_i terms live
+// in this file-scope device array instead of a caller-provided workspace.
+// Every device that loads the library holds it (16 MiB) until the process
+// exits.  In host code the symbol is only a stand-in, so its device address is
+// looked up once per device (with that device current) and passed to kernels.
+constexpr size_t kNoAllocDeltaFloats = size_t(1) << 22;   // 4,194,304 rows
+static __device__ __align__(256) float g_noalloc_delta[kNoAllocDeltaFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+float* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(ULYSSES_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return set_error(ULYSSES_ERR_UNSUPPORTED, "device %d beyond %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_delta);
+    if (e != cudaSuccess || p == nullptr)
+      return set_error(ULYSSES_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return ULYSSES_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -234,6 +265,34 @@ int ulysses_attn_bwd(const void* q_h, const void* k_h, const void* v_h, const vo
     return set_error(ULYSSES_ERR_INVALID, "buffers must be 16-byte aligned");
   a.q = q_h; a.k = k_h; a.v = v_h; a.o = o_h; a.dO = do_h; a.lse_in = lse;
   a.dq = dq_h; a.dk = dk_h; a.dv = dv_h; a.delta = (float*)workspace;
+  return run_bwd(a, (cudaStream_t)stream);
+}
+
+int ulysses_attn_bwd_noalloc(const void* q_h, const void* k_h, const void* v_h, const void* o_h,
+                             const void* do_h, const float* lse, float* dq_h, float* dk_h, float* dv_h,
+                             int64_t S, int B, int H_q, int H_kv, int D, int P, int head_chunk,
+                             int stage, const int32_t* cu_seqlens, int num_docs, int causal,
+                             float scale, int dtype, void* stream) {
+  AttnArgs a;
+  int rc = attn_shape(a, S, B, H_q, H_kv, D, P, head_chunk, stage, cu_seqlens, num_docs, causal,
+                      scale, dtype);
+  if (rc) return rc;
+  if (S == 0) return ULYSSES_OK;
+  const size_t rows = (size_t)B * a.nq * S;
+  if (rows > kNoAllocDeltaFloats)
+    return set_error(ULYSSES_ERR_UNSUPPORTED,
+                     "attn_bwd_noalloc: B*heads*S = %zu rows exceeds the built-in scratch of %zu rows; "
+                     "use ulysses_attn_bwd with a workspace",
+                     rows, kNoAllocDeltaFloats);
+  if (!q_h || !k_h || !v_h || !o_h || !do_h || !lse || !dq_h || !dk_h || !dv_h)
+    return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  if (!aligned16(q_h) || !aligned16(k_h) || !aligned16(v_h) || !aligned16(o_h) || !aligned16(do_h) ||
+      !aligned16(dq_h) || !aligned16(dk_h) || !aligned16(dv_h))
+    return set_error(ULYSSES_ERR_INVALID, "buffers must be 16-byte aligned");
+  float* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
+  a.q = q_h; a.k = k_h; a.v = v_h; a.o = o_h; a.dO = do_h; a.lse_in = lse;
+  a.dq = dq_h; a.dk = dk_h; a.dv = dv_h; a.delta = scratch;
   return run_bwd(a, (cudaStream_t)stream);
 }
 

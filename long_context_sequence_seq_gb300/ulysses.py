@@ -49,6 +49,8 @@ def lib():
     L.ulysses_attn_bwd_workspace.restype = sz
     L.ulysses_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, i64, i32, i32,
                                    i32, i32, i32, i32, i32, vp, i32, i32, f32, i32, vp]
+    L.ulysses_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32,
+                                           i32, i32, i32, i32, vp, i32, i32, f32, i32, vp]
     L.ulysses_layer_workspace.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32]
     L.ulysses_layer_workspace.restype = sz
     L.ulysses_layer_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, vp,
@@ -165,6 +167,25 @@ def attn_bwd(q_h, k_h, v_h, o_h, do_h, lse, H_q, H_kv, P, head_chunk=None, stage
                                _p(dk), _p(dv), _p(workspace), workspace.numel(), S, B, H_q, H_kv,
                                D, P, head_chunk or 0, _stage(stage), cp, nd, int(bool(causal)),
                                float(scale or 0.0), _dtype_code(q_h), _stream(stream)))
+    return dq, dk, dv
+
+
+def attn_bwd_noalloc(q_h, k_h, v_h, o_h, do_h, lse, H_q, H_kv, P, head_chunk=None, stage=None,
+                     cu_seqlens=None, causal=True, scale=None, dq=None, dk=None, dv=None,
+                     stream=None):
+    """attn_bwd through the entry point that needs no workspace (the library's
+    built-in scratch holds D_i; see include/ulysses.h for its limit and the
+    rule that calls sharing it must not overlap on the GPU)."""
+    B, n, S, D = q_h.shape
+    dev = q_h.device
+    dq = torch.empty(q_h.shape, dtype=torch.float32, device=dev) if dq is None else dq
+    dk = torch.empty(k_h.shape, dtype=torch.float32, device=dev) if dk is None else dk
+    dv = torch.empty(v_h.shape, dtype=torch.float32, device=dev) if dv is None else dv
+    cp, nd = _cu(cu_seqlens)
+    _ck(lib().ulysses_attn_bwd_noalloc(_p(q_h), _p(k_h), _p(v_h), _p(o_h), _p(do_h), _p(lse),
+                                       _p(dq), _p(dk), _p(dv), S, B, H_q, H_kv, D, P,
+                                       head_chunk or 0, _stage(stage), cp, nd, int(bool(causal)),
+                                       float(scale or 0.0), _dtype_code(q_h), _stream(stream)))
     return dq, dk, dv
 
 
