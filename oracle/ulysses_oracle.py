@@ -402,33 +402,44 @@ def ulysses_attention_bwd(q_seq, k_seq, v_seq, do_seq, P, head_chunk=None, cu_se
 # Row- and column-local pieces for sampled checks at full size
 # ----------------------------------------------------------------------------
 
-def attn_rows(q_h, k_g, v_g, do_h, rows, cu_seqlens=None, causal=True, scale=None):
+def attn_rows(q_h, k_g, v_g, do_h, rows, cu_seqlens=None, causal=True, scale=None, row_group=16):
     """O_i, LSE_i and dQ_i for selected rows of one q head.
 
-    q_h/do_h: [S, D] of the q head, k_g/v_g: [S, D] of its kv head.  Each row
-    needs only its own keys, so the cost is O(S*D) per row.
+    q_h/do_h: [S, D] of the q head (or just the selected rows, [len(rows), D],
+    when their first dimension equals len(rows) < S), k_g/v_g: [S, D] of its
+    kv head.  Each row needs only its own keys (cost O(S*D) per row); rows
+    are taken ``row_group`` at a time over the union of their key ranges, as
+    ``attn_fwd`` does with its row blocks.
     """
-    S, D = q_h.shape
+    S = k_g.shape[0]
+    D = k_g.shape[1]
     sc = 1.0 / math.sqrt(D) if scale is None else float(scale)
     lo, hi = key_ranges(S, cu_seqlens, causal)
     rows = np.asarray(rows, dtype=np.int64)
-    O = np.zeros((len(rows), D))
+    compact = q_h.shape[0] == len(rows) and len(rows) < S
+    k64 = _as64(k_g)
+    v64 = _as64(v_g)
+    O = np.zeros((len(rows), v_g.shape[1]))
     LSE = np.zeros(len(rows))
     dQ = np.zeros((len(rows), D))
-    for n, i in enumerate(rows):
-        a, b = int(lo[i]), int(hi[i])
-        kk = _as64(k_g[a:b])
-        vv = _as64(v_g[a:b])
-        s = sc * (kk @ _as64(q_h[i]))
-        m = s.max()
-        e = np.exp(s - m)
-        l = e.sum()
-        p = e / l
-        O[n] = p @ vv
-        LSE[n] = m + math.log(l)
-        dp = vv @ _as64(do_h[i])
-        Di = float(p @ dp)
-        dQ[n] = sc * ((p * (dp - Di)) @ kk)
+    for g0 in range(0, len(rows), row_group):
+        sel = np.arange(g0, min(len(rows), g0 + row_group))
+        r = rows[sel]
+        qq = _as64(q_h[sel] if compact else q_h[r])
+        dd = _as64(do_h[sel] if compact else do_h[r])
+        a, b = int(lo[r].min()), int(hi[r].max())
+        j = np.arange(a, b)
+        allowed = (j[None, :] >= lo[r, None]) & (j[None, :] < hi[r, None])
+        s = np.where(allowed, sc * (qq @ k64[a:b].T), -np.inf)
+        m = s.max(axis=1)
+        e = np.exp(s - m[:, None])
+        l = e.sum(axis=1)
+        p = e / l[:, None]
+        O[sel] = p @ v64[a:b]
+        LSE[sel] = m + np.log(l)
+        dp = dd @ v64[a:b].T
+        Di = np.sum(p * dp, axis=1)
+        dQ[sel] = sc * ((p * (dp - Di[:, None])) @ k64[a:b])
     return O, LSE, dQ
 
 

@@ -363,9 +363,13 @@ def test_row_and_tail_pieces_agree_with_full():
     dq, dk, dv = O.attn_bwd(q, k, v, do, cu)
     rows = [0, 19, 20, 21, 33, 49]
     for h in range(Hq):
-        ro, rl, rdq = O.attn_rows(q[h], k[0], v[0], do[h], rows, cu)
-        np.testing.assert_allclose(ro, o[h, rows], atol=1e-13)
-        np.testing.assert_allclose(rl, lse[h, rows], atol=1e-13)
+        for group in (1, 4, 16):
+            ro, rl, rdq = O.attn_rows(q[h], k[0], v[0], do[h], rows, cu, row_group=group)
+            np.testing.assert_allclose(ro, o[h, rows], atol=1e-13)
+            np.testing.assert_allclose(rl, lse[h, rows], atol=1e-13)
+            np.testing.assert_allclose(rdq, dq[h, rows], atol=1e-13)
+        # compact form: only the selected rows of q/dO are passed
+        ro, rl, rdq = O.attn_rows(q[h][rows], k[0], v[0], do[h][rows], rows, cu)
         np.testing.assert_allclose(rdq, dq[h, rows], atol=1e-13)
     tk, tv = O.attn_kv_tail(q, k[0], v[0], do, 30, cu, row_block=7)
     np.testing.assert_allclose(tk, dk[0, 30:], atol=1e-12)
