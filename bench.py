@@ -148,7 +148,12 @@ class LayerStep:
         U, w = self.U, self.w
         C, G = w.head_chunk, w.G
         ev = []
+        hq = w.H_q // w.P
         for st in range(self.stages):
+            r, c = divmod(st, hq // C)
+            h0 = r * hq + c * C
+            # B == 1: the stage's rows of the global [B, H_q, S] LSE are contiguous
+            lse_st = self.lse[:, h0:h0 + C] if w.B == 1 else self.lseh
             U.seq2head(self.q, w.P, C, st, out=self.qh)
             U.seq2head(self.k, w.P, C // G, st, out=self.kh)
             U.seq2head(self.v, w.P, C // G, st, out=self.vh)
@@ -157,7 +162,7 @@ class LayerStep:
             if timed:
                 e0.record()
             U.attn_fwd(self.qh, self.kh, self.vh, w.H_q, w.H_kv, w.P, C, st, self.cu, w.causal,
-                       out=self.oh, lse=self.lseh)
+                       out=self.oh, lse=lse_st)
             if timed:
                 e1.record()
             U.head2seq(self.oh, self.o, w.P, C, st)
@@ -166,7 +171,7 @@ class LayerStep:
             e3 = torch.cuda.Event(enable_timing=True) if timed else None
             if timed:
                 e2.record()
-            U.attn_bwd(self.qh, self.kh, self.vh, self.oh, self.doh, self.lseh, w.H_q, w.H_kv,
+            U.attn_bwd(self.qh, self.kh, self.vh, self.oh, self.doh, lse_st, w.H_q, w.H_kv,
                        w.P, C, st, self.cu, w.causal, workspace=self.ws, dq=self.dqh,
                        dk=self.dkh, dv=self.dvh)
             if timed:
