@@ -9,21 +9,23 @@
 //   O'   = O 2^{m-m'} + sum_j 2^{s_ij-m'} v_j,   O_i = O/l,  LSE_i = (m + log2 l) ln 2
 //
 // One CTA per (q head, 128-row query tile); warp roles:
-//   warp 0      TMA producer: Q once, then K_j / V_j tiles into a 4-slot ring
-//   warp 1      TMEM owner and MMA issuer (one elected lane):
-//                 S_j = Q K_j^T      (tcgen05.mma, SS, fp32 accumulate in TMEM)
-//                 O  += P_j V_j      (tcgen05.mma, A = P from TMEM as bf16)
+//   warp 0      TMA producer: Q once, then K_j into a 3-slot K ring and V_j
+//               into a 3-slot V ring, K one tile ahead (K0 K1 V0 K2 V1 ...)
+//   warp 1      TMEM owner; issues S_j = Q K_j^T (tcgen05.mma SS, fp32 in TMEM)
+//   warp 2      issues O += P_j V_j (tcgen05.mma, A = P from TMEM as bf16)
 //   warps 4-7   softmax: one thread per query row (TMEM lane), reads S_j with
 //               tcgen05.ld, masks, exponentiates (ex2), writes P_j over S_j as
-//               bf16, rescales O in TMEM when the running max grows, and runs
-//               the epilogue (O/l to global memory, LSE).
-// S is double-buffered in TMEM, so Q K_{j+1}^T runs on the tensor pipe while
-// the softmax warps work on tile j.
+//               bf16, rescales O in TMEM when the running max has grown by more
+//               than 2^8, and runs the epilogue (O/l to global memory, LSE).
+// The MMA warps run their issue code warp-wide and let one elected lane issue
+// (a lane-0 branch makes the issuing thread, not the tensor pipe, the limit).
+// S is triple-buffered in TMEM, so QK_{j+1} and QK_{j+2} can run on the tensor
+// pipe while the softmax works on tile j, and PV_j overlaps softmax j+1.
 //
-// TMEM columns (512 allocated): S/P buffer 0 [0,128), buffer 1 [128,256),
-// O accumulator [256, 256+D).
-// Shared memory: Q tile (D/64 swizzle-128B chunks of 128 rows) + a ring of
-// four 128 x D tiles holding K and V in load order K0 V0 K1 V1 ...
+// TMEM columns (512 allocated): S/P buffers [0,128), [128,256), [256,384);
+// O accumulator [384, 384+D).
+// Shared memory: Q tile (D/64 swizzle-128B chunks of 128 rows) + the K ring
+// and the V ring, three 128 x D tiles each (224 KB in all for D = 128).
 //
 // Masks: row i sees keys [lo_i, hi_i) = [start of its document, i+1) (causal)
 // or the whole document; a CTA walks keys from its first row's document start
@@ -43,11 +45,15 @@ using namespace tc;
 
 constexpr int BM = 128;      // query rows per CTA
 constexpr int BN = 128;      // keys per tile
-constexpr int NSLOT = 4;     // K/V ring slots
+constexpr int NRING = 3;     // slots in each of the K ring and the V ring
+constexpr int NSLOT = 2 * NRING;
+constexpr int NSBUF = 3;     // S/P buffers in TMEM (QK runs two tiles ahead)
+constexpr uint32_t kColO = NSBUF * BN;   // O accumulator columns [kColO, kColO + D)
 constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleLog2 = 8.f;   // lazy-rescale threshold (log2 units)
 
 template <int D>
 struct FwdLayout {
@@ -58,8 +64,8 @@ struct FwdLayout {
   static constexpr int kQ = 0;
   static constexpr int kKV = kQ + kTileQ;
   static constexpr int kBar = kKV + NSLOT * kTileKV;
-  // q_full, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], p_full[2], o_done, drain
-  static constexpr int kNumBar = 1 + 2 * NSLOT + 2 + 2 + 1 + 1;
+  // q_full, k_full/v_full[NRING], k_empty/v_empty[NRING], s_full[NSBUF], p_full[NSBUF], drain[2]
+  static constexpr int kNumBar = 1 + 4 * NRING + 2 * NSBUF + 2;
   static constexpr int kMisc = kBar + kNumBar * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;        // slack for 1024-byte alignment
@@ -79,12 +85,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sKV = smem + L::kKV;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
   uint64_t* q_full = bars;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = kv_full + NSLOT;
-  uint64_t* s_full = kv_empty + NSLOT;
-  uint64_t* p_full = s_full + 2;
-  uint64_t* o_done = p_full + 2;
-  uint64_t* drain = o_done + 1;
+  uint64_t* k_full = bars + 1;
+  uint64_t* v_full = k_full + NRING;
+  uint64_t* k_empty = v_full + NRING;
+  // v_empty[j % NRING] completes when PV_j has run: it frees V_j's slot and
+  // also tells the softmax that O holds PV_j (so it may rescale or read O)
+  uint64_t* v_empty = k_empty + NRING;
+  uint64_t* s_full = v_empty + NRING;
+  uint64_t* p_full = s_full + NSBUF;
+  uint64_t* drain = p_full + NSBUF;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -96,10 +105,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < NSLOT; ++s) { mbar_init(&kv_full[s], 1); mbar_init(&kv_empty[s], 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&s_full[b], 1); mbar_init(&p_full[b], 4); }
-    mbar_init(o_done, 1);
-    mbar_init(drain, 1);
+    for (int s = 0; s < 4 * NRING; ++s) mbar_init(&k_full[s], 1);   // k/v full, k/v empty
+    for (int b = 0; b < NSBUF; ++b) { mbar_init(&s_full[b], 1); mbar_init(&p_full[b], 4); }
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -129,74 +138,85 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       mbar_expect_tx(q_full, L::kTileQ);
       for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * L::kChunkQ, &tmQ, c * 64, (int)q0, n, q_full);
-      for (int idx = 0; idx < 2 * n_kv; ++idx) {
-        const int j = idx >> 1, slot = idx % NSLOT;
-        const uint32_t round = idx / NSLOT;
-        if (!mbar_wait(&kv_empty[slot], (round & 1) ^ 1, abort_flag)) break;
-        mbar_expect_tx(&kv_full[slot], L::kTileKV);
-        const int k0 = (int)(kv_lo + (int64_t)j * BN);
-        uint8_t* dst = sKV + slot * L::kTileKV;
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(dst + c * L::kChunkKV, (idx & 1) ? &tmV : &tmK, c * 64, k0, kvh, &kv_full[slot]);
-      }
+      // K tiles into the K ring (slot freed by QK_j), V tiles into the V ring
+      // (freed by PV_j); K runs one tile ahead: K0 K1 V0 K2 V1 ...
+      bool go = true;
+      for (int t = 0; go && t <= n_kv; ++t)
+        for (int kv = 0; kv < 2; ++kv) {
+          const int j = kv ? t - 1 : t;
+          if (j < 0 || j >= n_kv) continue;
+          const int r = j % NRING;
+          uint64_t* empty = kv ? &v_empty[r] : &k_empty[r];
+          uint64_t* full = kv ? &v_full[r] : &k_full[r];
+          if (!mbar_wait(empty, ((uint32_t)(j / NRING) & 1u) ^ 1u, abort_flag)) { go = false; break; }
+          mbar_expect_tx(full, L::kTileKV);
+          const int k0 = (int)(kv_lo + (int64_t)j * BN);
+          uint8_t* dst = sKV + (kv * NRING + r) * L::kTileKV;
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(dst + c * L::kChunkKV, kv ? &tmV : &tmK, c * 64, k0, kvh, full);
+        }
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
-    constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
-    const uint32_t q_addr = smem_u32(sQ);
-    bool ok = mbar_wait(q_full, 0, abort_flag);
-
-    const uint64_t qdesc = sdesc_sw128(q_addr, 16, 1024);
-    auto issue_qk = [&](int j) -> bool {
-      const int idx = 2 * j, slot = idx % NSLOT;
-      const uint32_t round = idx / NSLOT;
-      if (!mbar_wait(&kv_full[slot], round & 1, abort_flag)) return false;
-      tc_fence_after();
-      if (lane == 0) {
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two issuing warps keep the tensor pipe fed: warp 1 issues S_j = Q K_j^T,
+    // warp 2 issues O += P_j V_j.  The whole warp runs the issue code
+    // (warp-uniform operands); the *_w helpers let one elected lane issue.
+    // MMAs of different warps are not ordered with respect to each other, so
+    // every cross-warp dependency goes through an mbarrier:
+    //   QK_j   waits K_j loaded, and (j >= NSBUF) v_empty of PV_{j-NSBUF}: the
+    //          S/P buffer it overwrites has been read by that PV;
+    //   PV_j   waits P_j written (p_full) and V_j loaded; PV_j after PV_{j-1}
+    //          on O is ordered by issue order within warp 2.
+    // S is NSBUF-buffered, so QK runs up to NSBUF - 1 tiles ahead of the softmax.
+    bool ok = mbar_wait_warp(q_full, 0, abort_flag);
+    if (warp == 1) {
+      constexpr uint32_t idesc_qk = idesc_bf16(BM, BN, false, false);
+      const uint64_t qdesc = sdesc_sw128(smem_u32(sQ), 16, 1024);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int slot = j % NRING;
+        if (j >= NSBUF &&
+            !mbar_wait_warp(&v_empty[(j - NSBUF) % NRING], ((j - NSBUF) / NRING) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait_warp(&k_full[slot], (j / NRING) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
         const uint64_t kdesc = sdesc_sw128(smem_u32(sKV + slot * L::kTileKV), 16, 1024);
-        const uint32_t d_tmem = tbase + (uint32_t)(j & 1) * BN;
+        const uint32_t d_tmem = tbase + (uint32_t)(j % NSBUF) * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           // K-major: 16 features = 32 bytes along the swizzled row, 64-feature chunks apart
           const uint32_t off = (kk >> 2) * L::kChunkQ + (kk & 3) * 32;
           const uint32_t offk = (kk >> 2) * L::kChunkKV + (kk & 3) * 32;
-          mma_ss(d_tmem, sdesc_add(qdesc, off), sdesc_add(kdesc, offk), idesc_qk, kk > 0 ? 1u : 0u);
+          mma_ss_w(d_tmem, sdesc_add(qdesc, off), sdesc_add(kdesc, offk), idesc_qk, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[j & 1]);
-        mma_commit(&kv_empty[slot]);
+        mma_commit_w(&s_full[j % NSBUF]);
+        mma_commit_w(&k_empty[slot]);
       }
-      __syncwarp();
-      return true;
-    };
-
-    if (ok && n_kv > 0) ok = issue_qk(0);
-    for (int j = 0; ok && j < n_kv; ++j) {
-      if (j + 1 < n_kv && !issue_qk(j + 1)) { ok = false; break; }
-      if (!mbar_wait(&p_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
-      const int idx = 2 * j + 1, slot = idx % NSLOT;
-      const uint32_t round = idx / NSLOT;
-      if (!mbar_wait(&kv_full[slot], round & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      if (lane == 0) {
+      // drain: nothing of ours may still be in flight at teardown
+      mma_commit_w(&drain[0]);
+      mbar_wait(&drain[0], 0, nullptr);
+    } else {
+      constexpr uint32_t idesc_pv = idesc_bf16(BM, D, false, true);
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int r = j % NRING;
+        if (!mbar_wait_warp(&p_full[j % NSBUF], (j / NSBUF) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(&v_full[r], (j / NRING) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
         // V as the MN-major B operand: 16 keys = two 8-row groups (1024 B apart),
         // 64-wide D chunks L::kChunkKV apart.
-        const uint64_t vdesc = sdesc_sw128(smem_u32(sKV + slot * L::kTileKV), L::kChunkKV, 1024);
-        const uint32_t p_tmem = tbase + (uint32_t)(j & 1) * BN;
+        const uint64_t vdesc = sdesc_sw128(smem_u32(sKV + (NRING + r) * L::kTileKV), L::kChunkKV, 1024);
+        const uint32_t p_tmem = tbase + (uint32_t)(j % NSBUF) * BN;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ts(tbase + 256, p_tmem + kk * 8, sdesc_add(vdesc, kk * 2048), idesc_pv,
-                 (j > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(o_done);
-        mma_commit(&kv_empty[slot]);
+          mma_ts_w(tbase + kColO, p_tmem + kk * 8, sdesc_add(vdesc, kk * 2048), idesc_pv,
+                   (j > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_w(&v_empty[r]);
       }
-      __syncwarp();
+      mma_commit_w(&drain[1]);
+      mbar_wait(&drain[1], 0, nullptr);
     }
-    // drain: nothing of ours may still be in flight at teardown
-    if (lane == 0) mma_commit(drain);
-    __syncwarp();
-    mbar_wait(drain, 0, nullptr);
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax
     const int wq = warp & 3;
@@ -209,80 +229,95 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      if (!mbar_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&s_full[j % NSBUF], (j / NSBUF) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t sbuf = tbase + lane_off + (uint32_t)(j & 1) * BN;
+      const uint32_t sbuf = tbase + lane_off + (uint32_t)(j % NSBUF) * BN;
       uint32_t sv[BN / 32][32];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) tmem_ld32(sbuf + c * 32, sv[c]);
       tmem_ld_wait();
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) reg_fence(sv[c]);
+      // the row's keys as columns [clo, chi) of this tile
       const int64_t k0 = kv_lo + (int64_t)j * BN;
-      float mt = -INFINITY;
-      if (k0 >= lo && k0 + BN <= hi) {
-#pragma unroll
-        for (int c = 0; c < BN / 32; ++c)
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(sv[c][e]));
-      } else {
+      const int64_t dlo = lo - k0, dhi = hi - k0;
+      const int clo = dlo <= 0 ? 0 : (dlo >= BN ? BN : (int)dlo);
+      const int chi = dhi <= 0 ? 0 : (dhi >= BN ? BN : (int)dhi);
+      if (!(clo == 0 && chi == BN)) {     // the tile crosses this row's key bounds
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const int64_t kj = k0 + c * 32 + e;
-            const float x = (kj >= lo && kj < hi) ? __uint_as_float(sv[c][e]) : -INFINITY;
-            sv[c][e] = __float_as_uint(x);
-            mt = fmaxf(mt, x);
+            const int col = c * 32 + e;
+            if (col < clo || col >= chi) sv[c][e] = __float_as_uint(-INFINITY);
           }
       }
-      const float m_new = fmaxf(m, mt * sl2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m - m_use);
-      float rs = 0.f;
+      // row max over the tile: three-input max, four independent partial maxima
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c)
+#pragma unroll
+        for (int e = 0; e < 32; e += 8) {
+          float& q = mx[(e >> 3) & 3];
+          q = max3f(q, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]));
+          q = max3f(q, __uint_as_float(sv[c][e + 2]), __uint_as_float(sv[c][e + 3]));
+          q = max3f(q, __uint_as_float(sv[c][e + 4]), __uint_as_float(sv[c][e + 5]));
+          q = max3f(q, __uint_as_float(sv[c][e + 6]), __uint_as_float(sv[c][e + 7]));
+        }
+      const float mt = fmaxf(max3f(mx[0], mx[1], mx[2]), mx[3]);
+      // lazy rescale: keep the running max until a row's max grows by more
+      // than 2^kRescaleLog2 (it is only a stabiliser: O = acc / l and
+      // LSE = (m + log2 l) ln 2 stay exact for any m, and P stays <= 2^8)
+      const float m_cand = fmaxf(m, mt * sl2);
+      const bool upd = m_cand > m + kRescaleLog2;       // also true when m is still -inf
+      const float m_next = upd ? m_cand : m;
+      const float m_use = (m_next == -INFINITY) ? 0.f : m_next;
+      const float alpha = upd ? ex2(m - m_use) : 1.f;
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[BN / 64][32];
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c)
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(sv[c][e]), sl2, -m_use));
-          const float p1 = ex2(fmaf(__uint_as_float(sv[c][e + 1]), sl2, -m_use));
-          rs += p0 + p1;
+          float a0, a1;
+          fma2f(a0, a1, __uint_as_float(sv[c][e]), __uint_as_float(sv[c][e + 1]), sl2, -m_use);
+          const float p0 = ex2(a0), p1 = ex2(a1);
+          rs[(e >> 1) & 3] += p0 + p1;
           pk[c >> 1][(c & 1) * 16 + (e >> 1)] = pack_bf16(p0, p1);
         }
-      l = l * alpha + rs;
+      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c) tmem_st32(sbuf + c * 32, pk[c]);
       if (j > 0) {
         // O must hold PV_{j-1} before it is rescaled for tile j
-        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(&v_empty[(j - 1) % NRING], ((j - 1) / NRING) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
-            tmem_ld32(tbase + lane_off + 256 + c * 32, ov);
+            tmem_ld32(tbase + lane_off + kColO + c * 32, ov);
             tmem_ld_wait();
             reg_fence(ov);
 #pragma unroll
             for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(tbase + lane_off + 256 + c * 32, ov);
+            tmem_st32(tbase + lane_off + kColO + c * 32, ov);
           }
         }
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[j & 1]);
-      m = m_new;
+      if (lane == 0) mbar_arrive(&p_full[j % NSBUF]);
+      m = m_next;
     }
-    if (ok && n_kv > 0 && mbar_wait(o_done, (n_kv - 1) & 1, abort_flag)) {
+    if (ok && n_kv > 0 && mbar_wait_warp(&v_empty[(n_kv - 1) % NRING], ((n_kv - 1) / NRING) & 1, abort_flag)) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld32(tbase + lane_off + 256 + c * 32, ov);
+        tmem_ld32(tbase + lane_off + kColO + c * 32, ov);
         tmem_ld_wait();
         reg_fence(ov);
         if (valid) {
