@@ -23,17 +23,22 @@
 //   dK  += dS^T Q_i            (A = dS^T from TMEM, B = Q_i, MN-major)
 //   dQ_i^T = K^T dS^T          (M = D, N = 64 queries; A = K, MN-major;
 //                               B = dS^T from shared memory, MN-major)
-// The gradient warps then read dQ_i^T out of TMEM (lane = feature d) and
+// Four readout warps then read dQ_i^T out of TMEM (lane = feature d) and
 // write scale * dQ_i as [query][feature] fp32 rows into the tile's consumed
 // Q/dO stage buffers; a flusher warp adds them into dQ with TMA bulk
-// reduce-adds (cp.reduce.async.bulk) and then releases the stage.
+// reduce-adds (cp.reduce.async.bulk) and then releases the stage.  Those fp32
+// reductions into L2 (32 KB per tile) bound this kernel at long S.
 //
-// Warp roles (384 threads): 0 TMA producer, 1 TMEM owner and MMA issuer,
-// 2 LSE/D_i loader, 3 dQ flusher, 4-11 gradient warps: two per TMEM lane
-// quarter, each taking 32 of the tile's 64 queries (thread = key row for
-// P/dS, feature for the dQ readout).  TMEM columns: dV [0,128), dK [128,256), two
+// Warp roles (512 threads): 0 TMA producer, 1 TMEM owner and MMA issuer (whole
+// warp runs the issue code, one elected lane issues), 2 LSE/D_i loader, 3 dQ
+// flusher, 4-7 dQ^T readout (one per TMEM lane quarter), 8-15 gradient warps:
+// two per lane quarter, each taking 32 of the tile's 64 queries (thread = key
+// row).  Warpgroups 0-1 run on 112 registers per thread and give the rest to
+// the gradient warpgroups (144).  TMEM columns: dV [0,128), dK [128,256), two
 // S^T/P^T buffers [256,384) that also receive each tile's dQ^T, two
 // dP^T/dS^T buffers [384,512).
+#include <type_traits>
+
 #include "internal.h"
 #include "tc_ptx.cuh"
 
@@ -49,8 +54,13 @@ constexpr int BN = 128;     // keys per CTA
 constexpr int BMQ = 64;     // queries per inner tile
 constexpr int D = 128;
 constexpr int NSTAGE = 4;   // Q/dO/LSE/D_i ring (a consumed stage also stages its dQ tile)
-constexpr int kThreads = 384;
-constexpr int kGradWarps = 8;   // warps 4..11: two per TMEM lane quarter, one per 32-query half
+constexpr int kThreads = 512;
+constexpr int kReadWarps = 4;   // warps 4..7: dQ^T readout, one per TMEM lane quarter
+constexpr int kGradWarps = 8;   // warps 8..15: two per TMEM lane quarter, one per 32-query half
+// Register budgets: warpgroups 0-1 give registers back, 2-3 (gradient) take
+// them: 2 * 128 * kRegsLow + 2 * 128 * kRegsHigh = 128 (launch) * 512 threads.
+constexpr uint32_t kRegsLow = 112, kRegsHigh = 144;
+static_assert(2 * 128 * kRegsLow + 2 * 128 * kRegsHigh == 128 * kThreads, "register split");
 constexpr uint32_t kTmemCols = 512;
 // TMEM: dV, dK accumulators; two S^T/P^T buffers (each later reused for the
 // tile's dQ^T); two dP^T/dS^T buffers.
@@ -158,14 +168,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < NSTAGE; ++s) {
       mbar_init(&q_full[s], 2);
       mbar_init(&q_empty[s], 1);
-      mbar_init(&stg_full[s], kGradWarps);
+      mbar_init(&stg_full[s], kReadWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&ds_full[b], kGradWarps);
       mbar_init(&dq_full[b], 1);
     }
-    mbar_init(dq_empty, kGradWarps);
+    mbar_init(dq_empty, kReadWarps);
     mbar_init(dsm_free, 1);
     mbar_init(fin, 1);
     mbar_init(drain, 1);
@@ -183,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  if (warp < 8) regs_dec<kRegsLow>(); else regs_inc<kRegsHigh>();
 
   // Query rows that can see this key block: [q_lo, q_hi), q_lo rounded down
   // to the query tile so every tile starts on a 64-row boundary.
@@ -221,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSTAGE;
       const uint32_t round = it / NSTAGE;
-      if (!mbar_wait(&q_empty[st], (round & 1) ^ 1, abort_flag)) break;
+      if (!mbar_wait_warp(&q_empty[st], (round & 1) ^ 1, abort_flag)) break;
       const int n = kvh * G + it / n_qb;
       const int64_t q0 = q_lo + (int64_t)(it % n_qb) * BMQ;
       float* stat = sStat + st * 2 * BMQ;
@@ -246,11 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto issue_scores = [&](int it) -> bool {
       const int st = it % NSTAGE;
       const uint32_t round = it / NSTAGE;
-      if (!mbar_wait(&q_full[st], round & 1, abort_flag)) return false;
+      if (!mbar_wait_warp(&q_full[st], round & 1, abort_flag)) return false;
       // S buffer of this parity held dQ^T_{it-2}: its readout must be done
-      if (it >= 2 && !mbar_wait(dq_empty, (it - 2) & 1, abort_flag)) return false;
+      if (it >= 2 && !mbar_wait_warp(dq_empty, (it - 2) & 1, abort_flag)) return false;
       tc_fence_after();
-      if (lane == 0) {
+      {
         const uint64_t qd = sdesc_sw128(smem_u32(sQ + st * L::kTileQ), 16, 1024);
         const uint64_t dod = sdesc_sw128(smem_u32(sDO + st * L::kTileQ), 16, 1024);
         const uint32_t b = (uint32_t)(it & 1);
@@ -259,23 +270,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off_kv = (kk >> 2) * L::kChunkKV + (kk & 3) * 32;
           const uint32_t off_q = (kk >> 2) * L::kChunkQ + (kk & 3) * 32;
-          mma_ss(tbase + kColS + b * BMQ, sdesc_add(kd_k, off_kv), sdesc_add(qd, off_q), id_s, kk > 0 ? 1u : 0u);
-          mma_ss(tbase + kColDP + b * BMQ, sdesc_add(vd_k, off_kv), sdesc_add(dod, off_q), id_s, kk > 0 ? 1u : 0u);
+          mma_ss_w(tbase + kColS + b * BMQ, sdesc_add(kd_k, off_kv), sdesc_add(qd, off_q), id_s, kk > 0 ? 1u : 0u);
+          mma_ss_w(tbase + kColDP + b * BMQ, sdesc_add(vd_k, off_kv), sdesc_add(dod, off_q), id_s, kk > 0 ? 1u : 0u);
         }
-        mma_commit(&s_full[b]);
+        mma_commit_w(&s_full[b]);
       }
       __syncwarp();
       return true;
     };
-    bool ok = mbar_wait(kv_full, 0, abort_flag);
+    bool ok = mbar_wait_warp(kv_full, 0, abort_flag);
     if (ok && n_it > 0) ok = issue_scores(0);
     for (int it = 0; ok && it < n_it; ++it) {
       if (it + 1 < n_it && !issue_scores(it + 1)) { ok = false; break; }
       const int st = it % NSTAGE;
       const uint32_t b = (uint32_t)(it & 1);
-      if (!mbar_wait(&ds_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&ds_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      if (lane == 0) {
+      {
         // B = dO_it / Q_it as MN-major: 16 queries per step (2048 B), 64-feature
         // chunks L::kChunkQ apart.
         const uint64_t dod = sdesc_sw128(smem_u32(sDO + st * L::kTileQ), L::kChunkQ, 1024);
@@ -284,27 +295,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         // dV and dK are independent: interleave per K step
 #pragma unroll
         for (int kk = 0; kk < BMQ / 16; ++kk) {
-          mma_ts(tbase + kColDV, tbase + kColS + b * BMQ + packed_col(kk), sdesc_add(dod, kk * 2048), id_g,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-          mma_ts(tbase + kColDK, tbase + kColDP + b * BMQ + packed_col(kk), sdesc_add(qd, kk * 2048), id_g,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_w(tbase + kColDV, tbase + kColS + b * BMQ + packed_col(kk), sdesc_add(dod, kk * 2048), id_g,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts_w(tbase + kColDK, tbase + kColDP + b * BMQ + packed_col(kk), sdesc_add(qd, kk * 2048), id_g,
+                   (it > 0 || kk > 0) ? 1u : 0u);
         }
         // dQ^T = K^T dS^T into S buffer b: A = K (MN-major, 64-feature chunks
         // L::kChunkKV apart), B = dS^T ([key][query] rows of 128 B); 16 keys per step.
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ss(tbase + kColS + b * BMQ, sdesc_add(kd_mn, kk * 2048), sdesc_add(dsd, kk * 2048), id_q,
-                 kk > 0 ? 1u : 0u);
-        mma_commit(&dq_full[b]);
-        mma_commit(dsm_free);
+          mma_ss_w(tbase + kColS + b * BMQ, sdesc_add(kd_mn, kk * 2048), sdesc_add(dsd, kk * 2048), id_q,
+                   kk > 0 ? 1u : 0u);
+        mma_commit_w(&dq_full[b]);
+        mma_commit_w(dsm_free);
       }
       __syncwarp();
     }
-    if (lane == 0) {
-      mma_commit(fin);
-      mma_commit(drain);
-    }
-    __syncwarp();
+    mma_commit_w(fin);
+    mma_commit_w(drain);
     mbar_wait(drain, 0, nullptr);
   } else if (warp == 3) {
     // ------------------------------------------------------------ dQ flusher
@@ -329,13 +337,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       bulk_wait0();   // every dQ reduce has landed before the CTA retires
     }
     __syncwarp();
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ gradient warps
-    // Warp (4 + 4h + wq): TMEM lane quarter wq, query half h (columns
-    // [32h, 32h+32) of the 64-query tile).  Thread = key row jr for P^T/dS^T,
-    // and = feature d for the dQ^T readout (both TMEM lane wq*32 + lane).
+  } else if (warp < 4 + kReadWarps) {
+    // ------------------------------------------------------------ dQ^T readout
+    // Warp 4 + wq: TMEM lane quarter wq = features [32wq, 32wq+32).  dQ^T of
+    // tile x (in S buffer x & 1) -> scale * dQ as [query][feature] fp32 rows in
+    // tile x's consumed Q buffer (queries 0-31) and dO buffer (queries 32-63);
+    // the flusher warp adds them into dQ.  Running beside the gradient warps,
+    // this frees the S buffer for the next scores as early as possible.
     const int wq = warp & 3;
-    const int h = (warp - 4) >> 2;
+    const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+    const int d = wq * 32 + lane;
+    for (int x = 0; x < n_it; ++x) {
+      const uint32_t bx = (uint32_t)(x & 1);
+      const int sx = x % NSTAGE;
+      if (!mbar_wait_warp(&dq_full[bx], (x >> 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      uint32_t r0[32], r1[32];
+      tmem_ld32(tbase + lane_off + kColS + bx * BMQ, r0);
+      tmem_ld32(tbase + lane_off + kColS + bx * BMQ + 32, r1);
+      tmem_ld_wait();
+      reg_fence(r0);
+      reg_fence(r1);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_empty);
+      float* c0 = reinterpret_cast<float*>(sQ + sx * L::kTileQ) + d;
+      float* c1 = reinterpret_cast<float*>(sDO + sx * L::kTileQ) + d;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        c0[c * D] = __uint_as_float(r0[c]) * scale;
+        c1[c * D] = __uint_as_float(r1[c]) * scale;
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&stg_full[sx]);
+    }
+  } else {
+    // ------------------------------------------------------------ gradient warps
+    // Warp (8 + 4h + wq): TMEM lane quarter wq, query half h (columns
+    // [32h, 32h+32) of the 64-query tile).  Thread = key row jr for P^T/dS^T
+    // (TMEM lane wq*32 + lane).
+    const int wq = warp & 3;
+    const int h = (warp - 8) >> 2;
     const int jr = wq * 32 + lane;
     const int64_t j = k0 + jr;
     int64_t qlo = 0, qhi = 0;
@@ -344,40 +387,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = scale * kLog2e;
     bool ok = true;
 
-    // dQ^T of tile x (in S buffer x & 1) -> scale * dQ rows [32h, 32h+32) of
-    // the tile written as [query][feature] fp32 rows into tile x's consumed
-    // Q (h = 0) or dO (h = 1) buffer; the flusher warp adds them into dQ.
-    auto readout = [&](int x) -> bool {
-      const uint32_t bx = (uint32_t)(x & 1);
-      const int sx = x % NSTAGE;
-      if (!mbar_wait(&dq_full[bx], (x >> 1) & 1, abort_flag)) return false;
-      tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32(tbase + lane_off + kColS + bx * BMQ + h * 32, r);
-      tmem_ld_wait();
-      reg_fence(r);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(dq_empty);
-      float* col = reinterpret_cast<float*>((h == 0 ? sQ : sDO) + sx * L::kTileQ) + jr;
-#pragma unroll
-      for (int c = 0; c < 32; ++c) col[c * D] = __uint_as_float(r[c]) * scale;
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&stg_full[sx]);
-      return true;
-    };
-
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSTAGE;
       const uint32_t round = it / NSTAGE;
       const uint32_t b = (uint32_t)(it & 1);
       const int64_t q0 = q_lo + (int64_t)(it % n_qb) * BMQ + h * 32;   // this half's first query
-      if (!mbar_wait(&q_full[st], round & 1, abort_flag)) { ok = false; break; }
-      if (!mbar_wait(&s_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&q_full[st], round & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&s_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const float* stat = sStat + st * 2 * BMQ + h * 32;
-      const bool full = (q0 >= qlo) && (q0 + 32 <= qhi);
+      // this row's queries as columns [clo, chi) of the half
+      const int64_t dlo = qlo - q0, dhi = qhi - q0;
+      const int clo = dlo <= 0 ? 0 : (dlo >= 32 ? 32 : (int)dlo);
+      const int chi = dhi <= 0 ? 0 : (dhi >= 32 ? 32 : (int)dhi);
       uint32_t sv[32], pv[32];
       tmem_ld32(tbase + lane_off + kColS + b * BMQ + h * 32, sv);
       tmem_ld32(tbase + lane_off + kColDP + b * BMQ + h * 32, pv);
@@ -385,32 +407,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence(sv);
       reg_fence(pv);
       uint32_t pp[16], dd[16];
+      // P^T = 2^(s * scale * log2 e - LSE_i log2 e), dS^T = P^T (dP^T - D_i).
+      // The mask test sits outside the loop so each version is one basic block
+      // and the compiler can put all LSE / D_i loads in flight at once.
+      auto grad_cols = [&](auto masked) {
 #pragma unroll
-      for (int col = 0; col < 32; col += 4) {
-        const float4 l4 = *reinterpret_cast<const float4*>(stat + col);
-        const float4 d4 = *reinterpret_cast<const float4*>(stat + BMQ + col);
-        const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-        const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
-        float p[4], g[4];
+        for (int col = 0; col < 32; col += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(stat + col);
+          const float4 d4 = *reinterpret_cast<const float4*>(stat + BMQ + col);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dl[4] = {d4.x, d4.y, d4.z, d4.w};
+          float p[4], g[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          p[u] = ex2(fmaf(__uint_as_float(sv[col + u]), sl2, -lv[u]));
-          if (!full) {
-            const int64_t i = q0 + col + u;
-            p[u] = (i >= qlo && i < qhi) ? p[u] : 0.f;
+          for (int u = 0; u < 4; ++u) {
+            p[u] = ex2(fmaf(__uint_as_float(sv[col + u]), sl2, -lv[u]));
+            if (decltype(masked)::value) p[u] = (col + u >= clo && col + u < chi) ? p[u] : 0.f;
+            g[u] = p[u] * (__uint_as_float(pv[col + u]) - dl[u]);
           }
-          g[u] = p[u] * (__uint_as_float(pv[col + u]) - dl[u]);
+          pp[col >> 1] = pack_bf16(p[0], p[1]);
+          pp[(col >> 1) + 1] = pack_bf16(p[2], p[3]);
+          dd[col >> 1] = pack_bf16(g[0], g[1]);
+          dd[(col >> 1) + 1] = pack_bf16(g[2], g[3]);
         }
-        pp[col >> 1] = pack_bf16(p[0], p[1]);
-        pp[(col >> 1) + 1] = pack_bf16(p[2], p[3]);
-        dd[col >> 1] = pack_bf16(g[0], g[1]);
-        dd[(col >> 1) + 1] = pack_bf16(g[2], g[3]);
-      }
+      };
+      if (clo == 0 && chi == 32)
+        grad_cols(std::false_type{});
+      else
+        grad_cols(std::true_type{});
       // bf16 pairs: 16 columns per half, inside the half's own 32 columns
       tmem_st16(tbase + lane_off + kColS + b * BMQ + h * 32, pp);
       tmem_st16(tbase + lane_off + kColDP + b * BMQ + h * 32, dd);
       // the dS^T tile in shared memory was last read by dQ^T_{it-1}
-      if (it >= 1 && !mbar_wait(dsm_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
+      if (it >= 1 && !mbar_wait_warp(dsm_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
       uint8_t* row = sDS + jr * 128;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -423,12 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ds_full[b]);
-      // the previous tile's dQ^T is (or soon will be) ready: flush it
-      if (it >= 1 && !readout(it - 1)) { ok = false; break; }
     }
-    if (ok && n_it > 0 && !readout(n_it - 1)) ok = false;
     // epilogue: half 0 writes dV, half 1 writes scale * dK of this key block
-    if (ok && n_it > 0 && mbar_wait(fin, 0, abort_flag)) {
+    if (ok && n_it > 0 && mbar_wait_warp(fin, 0, abort_flag)) {
       tc_fence_after();
       float* dst = (h == 0 ? dv : dk) + ((int64_t)kvh * S + j) * D;
       const float mul = h == 0 ? 1.f : scale;

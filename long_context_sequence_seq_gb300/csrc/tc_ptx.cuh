@@ -76,6 +76,18 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
 }
 
+// Per-warpgroup register budgets (all four warps of a warpgroup execute the
+// same instruction).  The increases are served from what the decreases give
+// back, so the budgets of a kernel must add up to its launch allocation.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // ----------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch(const CUtensorMap* map) {
