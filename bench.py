@@ -273,23 +273,52 @@ def e2e_measure(w, dev, cu_np, steps, warmup):
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv))
 
+    # Copies run on a second stream where the data allows: dO is uploaded
+    # under the forward, O is downloaded under the backward, and a step's
+    # dQ/dK/dV download overlaps the next step's Q/K/V upload (the two copy
+    # directions use separate engines).  Events order every buffer reuse.
+    main = torch.cuda.current_stream(dev)
+    cs = torch.cuda.Stream(device=dev)
+    ev = {name: torch.cuda.Event() for name in ("do_in", "fwd", "o_out", "bwd", "g_out")}
+    state = {"first": True}
+
     def step():
-        for d_, h_ in ((q, hq), (k, hk), (v, hv), (do, hdo)):
+        for d_, h_ in ((q, hq), (k, hk), (v, hv)):
             d_.copy_(h_, non_blocking=True)
+        cs.wait_stream(main)                      # the previous backward read dO
+        with torch.cuda.stream(cs):
+            do.copy_(hdo, non_blocking=True)
+            ev["do_in"].record(cs)
+        if not state["first"]:
+            main.wait_event(ev["o_out"])          # O of the previous step is on the host
         U.layer_fwd(q, k, v, w.P, w.head_chunk, cu, w.causal, workspace=ws, out=o, lse=lse)
+        ev["fwd"].record(main)
+        with torch.cuda.stream(cs):
+            cs.wait_event(ev["fwd"])
+            ho.copy_(o, non_blocking=True)
+            ev["o_out"].record(cs)
+        main.wait_event(ev["do_in"])
+        if not state["first"]:
+            main.wait_event(ev["g_out"])          # the previous gradients are on the host
         U.layer_bwd(q, k, v, o, do, lse, w.P, w.head_chunk, cu, w.causal, workspace=ws,
                     dq=dq, dk=dk, dv=dv)
-        for h_, d_ in ((ho, o), (hdq, dq), (hdk, dk), (hdv, dv)):
-            h_.copy_(d_, non_blocking=True)
+        ev["bwd"].record(main)
+        with torch.cuda.stream(cs):
+            cs.wait_event(ev["bwd"])
+            for h_, d_ in ((hdq, dq), (hdk, dk), (hdv, dv)):
+                h_.copy_(d_, non_blocking=True)
+            ev["g_out"].record(cs)
+        state["first"] = False
 
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record()
+    a.record(main)
     for _ in range(steps):
         step()
-    b.record()
+    main.wait_event(ev["g_out"])                  # the last step's results are on the host
+    b.record(main)
     torch.cuda.synchronize()
     U.check()
     t = a.elapsed_time(b) / 1e3 / steps
