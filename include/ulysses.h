@@ -93,6 +93,20 @@ int ulysses_seq2head(const void* x_seq, void* x_head, int64_t S, int B, int H, i
 int ulysses_head2seq(const void* x_head, void* x_seq, int64_t S, int B, int H, int D, int P,
                      int head_chunk, int stage, int dtype, void* stream);
 
+/* As ulysses_head2seq, but adds the head rows into x_seq instead of writing
+ * them (dtype must be ULYSSES_FP32).  Used for the gradients of a replicated
+ * kv head: every rank holding a copy contributes a partial dK/dV.
+ *
+ * KV-head replication (the sequence-parallel degree exceeding the kv head
+ * count, H < P with P % H == 0): rank r holds kv head r / (P / H), as when the
+ * heads are repeated P / H times before the all-to-all.  In this mode `stage`
+ * names the rank (0 <= stage < P), n = 1 and head_chunk is not used, for
+ * ulysses_seq2head, ulysses_head2seq and ulysses_head2seq_add alike.  The
+ * attention calls accept H_kv < P (P % H_kv == 0, H_q % P == 0); a stage's kv
+ * buffer then holds that single head. */
+int ulysses_head2seq_add(const void* x_head, void* x_seq, int64_t S, int B, int H, int D, int P,
+                         int head_chunk, int stage, int dtype, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Local attention forward (step 4) on head-layout buffers of one stage.
  *   q_h  [B][Cq][S][D],  k_h, v_h [B][Cq/G][S][D]   (Cq = head_chunk, or H_q

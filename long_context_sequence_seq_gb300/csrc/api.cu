@@ -78,8 +78,17 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Heads of a stage: n heads starting at h0.
 int stage_span(int H, int P, int C, int stage, int* n, int* h0) {
+  if (P > 0 && H > 0 && H < P && P % H == 0) {
+    // kv-head replication (H_kv < P): rank r holds head r / (P / H); `stage`
+    // names the rank and head_chunk is not used
+    if (stage < 0 || stage >= P)
+      return set_error(ULYSSES_ERR_INVALID, "with H=%d < P=%d, stage names a rank in [0,%d), got %d", H, P, P, stage);
+    *n = 1;
+    *h0 = stage / (P / H);
+    return ULYSSES_OK;
+  }
   if (P <= 0 || H <= 0 || H % P)
-    return set_error(ULYSSES_ERR_INVALID, "H=%d must be a positive multiple of P=%d", H, P);
+    return set_error(ULYSSES_ERR_INVALID, "H=%d must be a positive multiple of P=%d, or divide P", H, P);
   if (stage == -1) { *n = H; *h0 = 0; return ULYSSES_OK; }
   const int hq = H / P;
   if (C <= 0 || hq % C)
@@ -93,9 +102,11 @@ int stage_span(int H, int P, int C, int stage, int* n, int* h0) {
 }
 
 int relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, int D, int P,
-             int C, int stage, int dtype, void* stream) {
+             int C, int stage, int dtype, void* stream, bool add = false) {
   const int elt = elt_size(dtype);
   if (!elt) return set_error(ULYSSES_ERR_INVALID, "unknown dtype %d", dtype);
+  if (add && (to_head || dtype != ULYSSES_FP32))
+    return set_error(ULYSSES_ERR_UNSUPPORTED, "accumulating re-layout is head->seq, fp32 only");
   if (S < 0 || B <= 0 || D <= 0) return set_error(ULYSSES_ERR_INVALID, "bad sizes S=%lld B=%d D=%d", (long long)S, B, D);
   if (P <= 0 || S % P) return set_error(ULYSSES_ERR_INVALID, "S=%lld not divisible by P=%d", (long long)S, P);
   if ((D * elt) % 16)
@@ -110,7 +121,7 @@ int relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, 
   const char* a = (const char*)src; const char* b = (const char*)dst;
   size_t la = to_head ? seq_bytes : head_bytes, lb = to_head ? head_bytes : seq_bytes;
   if (a < b + lb && b < a + la) return set_error(ULYSSES_ERR_INVALID, "re-layout cannot run in place");
-  return launch_relayout(to_head, src, dst, S, B, H, D, n, h0, elt, (cudaStream_t)stream);
+  return launch_relayout(to_head, src, dst, S, B, H, D, n, h0, elt, (cudaStream_t)stream, add);
 }
 
 // Shape validation shared by attention calls; fills a (without pointers).
@@ -122,12 +133,16 @@ int attn_shape(AttnArgs& a, int64_t S, int B, int H_q, int H_kv, int D, int P, i
   if (H_q <= 0 || H_kv <= 0 || H_q % H_kv)
     return set_error(ULYSSES_ERR_INVALID, "H_q=%d must be a multiple of H_kv=%d", H_q, H_kv);
   if (P <= 0 || S % P) return set_error(ULYSSES_ERR_INVALID, "S=%lld not divisible by P=%d", (long long)S, P);
-  if (H_q % P || H_kv % P)
-    return set_error(ULYSSES_ERR_INVALID, "heads (H_q=%d, H_kv=%d) must divide evenly over P=%d", H_q, H_kv, P);
-  const int G = H_q / H_kv;
+  const bool rep_kv = H_kv < P;   // kv-head replication: rank r uses kv head r / (P / H_kv)
+  if (H_q % P || (rep_kv ? P % H_kv : H_kv % P))
+    return set_error(ULYSSES_ERR_INVALID,
+                     "heads (H_q=%d, H_kv=%d) must divide evenly over P=%d (or H_kv divide P)", H_q, H_kv, P);
   int nq = 0, h0 = 0;
   int rc = stage_span(H_q, P, C, stage, &nq, &h0);
   if (rc) return rc;
+  // a stage's kv buffer holds whole kv heads; with replication it holds the
+  // one kv head all of the rank's q heads use
+  const int G = rep_kv ? nq : H_q / H_kv;
   if (nq % G) return set_error(ULYSSES_ERR_INVALID, "head_chunk=%d must hold whole kv heads (G=%d)", nq, G);
   if (D != 64 && D != 128) return set_error(ULYSSES_ERR_UNSUPPORTED, "head dim %d not in {64,128}", D);
   if (cu && B > 1) return set_error(ULYSSES_ERR_UNSUPPORTED, "cu_seqlens needs B == 1");
@@ -161,6 +176,18 @@ int run_bwd(AttnArgs& a, cudaStream_t st) {
 }
 
 size_t delta_bytes(int64_t S, int B, int nq) { return align256((size_t)B * nq * S * sizeof(float)); }
+
+// Stage argument of a layer stage's K/V re-layout: the q stage itself, or,
+// with kv-head replication (H_kv < P), the rank the stage belongs to.
+int kv_stage(int H_kv, int P, int s, int stages) {
+  return H_kv < P ? s / (stages / P) : s;
+}
+// With replication: is stage s the first of the stages sharing its kv head?
+// (rank r uses kv head r / (P / H_kv); stages run in rank order)
+bool kv_first_stage(int H_kv, int P, int s, int stages) {
+  const int per_rank = stages / P, r = s / per_rank, R = P / H_kv;
+  return r % R == 0 && s % per_rank == 0;
+}
 
 struct LayerWs {
   char *qh, *kh, *vh, *oh, *doh; float *dqh, *dkh, *dvh, *delta; size_t total;
@@ -221,6 +248,11 @@ int ulysses_seq2head(const void* x_seq, void* x_head, int64_t S, int B, int H, i
 int ulysses_head2seq(const void* x_head, void* x_seq, int64_t S, int B, int H, int D, int P,
                      int head_chunk, int stage, int dtype, void* stream) {
   return relayout(false, x_head, x_seq, S, B, H, D, P, head_chunk, stage, dtype, stream);
+}
+
+int ulysses_head2seq_add(const void* x_head, void* x_seq, int64_t S, int B, int H, int D, int P,
+                         int head_chunk, int stage, int dtype, void* stream) {
+  return relayout(false, x_head, x_seq, S, B, H, D, P, head_chunk, stage, dtype, stream, true);
 }
 
 int ulysses_attn_fwd(const void* q_h, const void* k_h, const void* v_h, void* o_h, float* lse,
@@ -323,9 +355,10 @@ int ulysses_layer_fwd(const void* q_seq, const void* k_seq, const void* v_seq, v
   for (int s = 0; s < stages; ++s) {
     int n = 0, h0 = 0;
     stage_span(H_q, P, C, s, &n, &h0);
+    const int ks = kv_stage(H_kv, P, s, stages);
     if ((rc = relayout(true, q_seq, w.qh, S, B, H_q, D, P, C, s, dtype, stream))) return rc;
-    if ((rc = relayout(true, k_seq, w.kh, S, B, H_kv, D, P, Ckv, s, dtype, stream))) return rc;
-    if ((rc = relayout(true, v_seq, w.vh, S, B, H_kv, D, P, Ckv, s, dtype, stream))) return rc;
+    if ((rc = relayout(true, k_seq, w.kh, S, B, H_kv, D, P, Ckv, ks, dtype, stream))) return rc;
+    if ((rc = relayout(true, v_seq, w.vh, S, B, H_kv, D, P, Ckv, ks, dtype, stream))) return rc;
     AttnArgs sa = a;
     sa.q = w.qh; sa.k = w.kh; sa.v = w.vh; sa.o_out = w.oh;
     sa.lse = lse + (size_t)h0 * S;
@@ -359,9 +392,10 @@ int ulysses_layer_bwd(const void* q_seq, const void* k_seq, const void* v_seq, c
   for (int s = 0; s < stages; ++s) {
     int n = 0, h0 = 0;
     stage_span(H_q, P, C, s, &n, &h0);
+    const int ks = kv_stage(H_kv, P, s, stages);
     if ((rc = relayout(true, q_seq, w.qh, S, B, H_q, D, P, C, s, dtype, stream))) return rc;
-    if ((rc = relayout(true, k_seq, w.kh, S, B, H_kv, D, P, Ckv, s, dtype, stream))) return rc;
-    if ((rc = relayout(true, v_seq, w.vh, S, B, H_kv, D, P, Ckv, s, dtype, stream))) return rc;
+    if ((rc = relayout(true, k_seq, w.kh, S, B, H_kv, D, P, Ckv, ks, dtype, stream))) return rc;
+    if ((rc = relayout(true, v_seq, w.vh, S, B, H_kv, D, P, Ckv, ks, dtype, stream))) return rc;
     if ((rc = relayout(true, o_seq, w.oh, S, B, H_q, D, P, C, s, dtype, stream))) return rc;
     if ((rc = relayout(true, do_seq, w.doh, S, B, H_q, D, P, C, s, dtype, stream))) return rc;
     AttnArgs sa = a;
@@ -372,8 +406,11 @@ int ulysses_layer_bwd(const void* q_seq, const void* k_seq, const void* v_seq, c
     rc = use_tc_bwd(sa) ? launch_tc_bwd(sa, st) : launch_simt_bwd(sa, st);
     if (rc) return rc;
     if ((rc = relayout(false, w.dqh, dq_seq, S, B, H_q, D, P, C, s, ULYSSES_FP32, stream))) return rc;
-    if ((rc = relayout(false, w.dkh, dk_seq, S, B, H_kv, D, P, Ckv, s, ULYSSES_FP32, stream))) return rc;
-    if ((rc = relayout(false, w.dvh, dv_seq, S, B, H_kv, D, P, Ckv, s, ULYSSES_FP32, stream))) return rc;
+    // with kv-head replication every stage holds a partial dK/dV of its kv
+    // head: the head's first stage writes it, the later ones add to it
+    const bool add = H_kv < P && !kv_first_stage(H_kv, P, s, stages);
+    if ((rc = relayout(false, w.dkh, dk_seq, S, B, H_kv, D, P, Ckv, ks, ULYSSES_FP32, stream, add))) return rc;
+    if ((rc = relayout(false, w.dvh, dv_seq, S, B, H_kv, D, P, Ckv, ks, ULYSSES_FP32, stream, add))) return rc;
   }
   return ULYSSES_OK;
 }

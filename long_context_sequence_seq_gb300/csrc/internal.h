@@ -24,7 +24,7 @@ struct AttnArgs {
 };
 
 int launch_relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, int D,
-                    int n, int h0, int elt, cudaStream_t stream);
+                    int n, int h0, int elt, cudaStream_t stream, bool add = false);
 int launch_simt_fwd(const AttnArgs& a, cudaStream_t st);
 int launch_simt_bwd(const AttnArgs& a, cudaStream_t st);
 int launch_delta(const AttnArgs& a, cudaStream_t st);

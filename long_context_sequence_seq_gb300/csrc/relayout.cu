@@ -4,6 +4,8 @@
 //   seq layout  X_seq [B][S][H][D]  (P stacked rank chunks of S/P tokens)
 //   head layout X_head[B][n][S][D]  (the stage's n heads, every position)
 //   X_head[b][h'][t][:] = X_seq[b][t][h0 + h'][:]
+// The scatter also has an accumulating form (fp32), X_seq += X_head, which
+// sums the partial dK/dV of stages that share a replicated kv head.
 //
 // The unit moved is one D-vector (128-512 bytes), copied as 16-byte words, so
 // both the read and the write side are fully coalesced.  The kernel is a pure
@@ -24,7 +26,8 @@ __device__ __forceinline__ int4 ld_stream(const int4* p) {
 }
 
 // to_head = true:  seq -> head (gather)   to_head = false: head -> seq (scatter)
-template <bool kToHead>
+// kAdd (scatter only): add the fp32 head rows into the sequence rows
+template <bool kToHead, bool kAdd = false>
 __global__ void __launch_bounds__(256) relayout_kernel(const int4* __restrict__ src,
                                                        int4* __restrict__ dst, int64_t S,
                                                        int n, int H, int h0, int vec_per_row,
@@ -56,13 +59,25 @@ __global__ void __launch_bounds__(256) relayout_kernel(const int4* __restrict__ 
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (head_idx[u] < total_vecs) dst[kToHead ? head_idx[u] : seq_idx[u]] = val[u];
+      if (head_idx[u] < total_vecs) {
+        if (kAdd) {
+          int4* p = dst + seq_idx[u];
+          const int4 o = *p;
+          val[u] = make_int4(__float_as_int(__int_as_float(o.x) + __int_as_float(val[u].x)),
+                             __float_as_int(__int_as_float(o.y) + __int_as_float(val[u].y)),
+                             __float_as_int(__int_as_float(o.z) + __int_as_float(val[u].z)),
+                             __float_as_int(__int_as_float(o.w) + __int_as_float(val[u].w)));
+          *p = val[u];
+        } else {
+          dst[kToHead ? head_idx[u] : seq_idx[u]] = val[u];
+        }
+      }
     }
   }
 }
 
 int launch_relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, int D,
-                    int n, int h0, int elt, cudaStream_t stream) {
+                    int n, int h0, int elt, cudaStream_t stream, bool add) {
   const int row_bytes = D * elt;
   const int vec_per_row = row_bytes / 16;
   const int64_t total = (int64_t)B * n * S * vec_per_row;
@@ -76,6 +91,9 @@ int launch_relayout(bool to_head, const void* src, void* dst, int64_t S, int B, 
   int blocks = (int)(want < cap ? want : cap);
   if (to_head)
     relayout_kernel<true><<<blocks, threads, 0, stream>>>(
+        (const int4*)src, (int4*)dst, S, n, H, h0, vec_per_row, total);
+  else if (add)
+    relayout_kernel<false, true><<<blocks, threads, 0, stream>>>(
         (const int4*)src, (int4*)dst, S, n, H, h0, vec_per_row, total);
   else
     relayout_kernel<false><<<blocks, threads, 0, stream>>>(

@@ -43,6 +43,7 @@ def lib():
     vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.ulysses_seq2head.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
     L.ulysses_head2seq.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
+    L.ulysses_head2seq_add.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
     L.ulysses_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, i32,
                                    vp, i32, i32, f32, i32, vp]
     L.ulysses_attn_bwd_workspace.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32]
@@ -108,9 +109,10 @@ def _stage(stage):
 # --------------------------------------------------------------- re-layout
 
 def seq2head(x_seq, P, head_chunk=None, stage=None, out=None, stream=None):
-    """All-to-all #1: [B,S,H,D] -> [B,n,S,D] for the stage (all heads if None)."""
+    """All-to-all #1: [B,S,H,D] -> [B,n,S,D] for the stage (all heads if None).
+    With H < P (kv-head replication) `stage` names a rank and n = 1."""
     B, S, H, D = x_seq.shape
-    n = H if stage is None else head_chunk
+    n = H if stage is None else (1 if H < P else head_chunk)
     if out is None:
         out = torch.empty((B, n, S, D), dtype=x_seq.dtype, device=x_seq.device)
     _ck(lib().ulysses_seq2head(_p(x_seq), _p(out), S, B, H, D, P, head_chunk or 0,
@@ -126,6 +128,41 @@ def head2seq(x_head, x_seq, P, head_chunk=None, stage=None, stream=None):
     _ck(lib().ulysses_head2seq(_p(x_head), _p(x_seq), S, B, H, D, P, head_chunk or 0,
                                _stage(stage), _dtype_code(x_seq), _stream(stream)))
     return x_seq
+
+
+def head2seq_add(x_head, x_seq, P, head_chunk=None, stage=None, stream=None):
+    """As head2seq, adding into the fp32 sequence tensor (partial gradients of a
+    replicated kv head)."""
+    B, S, H, D = x_seq.shape
+    if x_head.dtype != x_seq.dtype:
+        raise TypeError("dtype mismatch")
+    _ck(lib().ulysses_head2seq_add(_p(x_head), _p(x_seq), S, B, H, D, P, head_chunk or 0,
+                                   _stage(stage), _dtype_code(x_seq), _stream(stream)))
+    return x_seq
+
+
+def pad_to_multiple(tensors, P, cu_seqlens=None):
+    """Pad [B,S,H,D] tensors along S to a multiple of P (as pad_to_multiple_of
+    does for sequence parallelism).  Returns (padded tensors, cu_seqlens, S):
+    the padding positions form a document of their own, so no real position
+    attends to them or is attended by them (S stays the caller's length for
+    slicing the results back).  cu_seqlens (int32, device) describes the real
+    documents, or None for one document; it is needed with B == 1 only."""
+    S = tensors[0].shape[1]
+    S_pad = (S + P - 1) // P * P
+    if S_pad == S:
+        return list(tensors), cu_seqlens, S
+    out = []
+    for t in tensors:
+        p = torch.zeros((t.shape[0], S_pad) + tuple(t.shape[2:]), dtype=t.dtype, device=t.device)
+        p[:, :S].copy_(t)
+        out.append(p)
+    dev = tensors[0].device
+    if cu_seqlens is None:
+        cu = torch.tensor([0, S, S_pad], dtype=torch.int32, device=dev)
+    else:
+        cu = torch.cat([cu_seqlens.to(torch.int32), torch.tensor([S_pad], dtype=torch.int32, device=dev)])
+    return out, cu, S
 
 
 # --------------------------------------------------------------- attention

@@ -84,3 +84,36 @@ def test_workspace_sizes(libpath):
     want = 3 * 8 * S * 128 * 2 + 2 * 2 * S * 128 * 2 + 8 * S * 128 * 4 + 2 * 2 * S * 128 * 4 + 8 * S * 4
     assert lw == want
     assert U.layer_workspace_bytes(S, 1, 32, 8, 128, 4, 3) == 0
+
+
+def test_kv_replication_validation(libpath):
+    """H_kv < P is accepted when H_kv divides P (rank r holds kv head
+    r / (P / H_kv)); other head counts are rejected before any launch."""
+    from long_context_sequence_seq_gb300 import ulysses as U
+    L = U.lib()
+    S = 4096
+    assert U.layer_workspace_bytes(S, 1, 8, 2, 128, 4, 2) > 0      # H_kv = 2 < P = 4
+    assert U.layer_workspace_bytes(S, 1, 8, 1, 128, 8, 1) > 0      # H_kv = 1, P = 8
+    assert U.layer_workspace_bytes(S, 1, 12, 3, 128, 4, 3) == 0    # P % H_kv != 0
+    dummy = ctypes.c_void_p(256)
+    # the rank must be named: stage -1 and stage >= P are rejected
+    assert L.ulysses_seq2head(dummy, ctypes.c_void_p(1 << 20), 32, 1, 2, 128, 4, 0, -1, U.BF16, None) == U.ERR_INVALID
+    assert L.ulysses_seq2head(dummy, ctypes.c_void_p(1 << 20), 32, 1, 2, 128, 4, 0, 4, U.BF16, None) == U.ERR_INVALID
+    # accumulating scatter: fp32 only
+    assert L.ulysses_head2seq_add(dummy, ctypes.c_void_p(1 << 20), 32, 1, 2, 128, 4, 0, 1, U.BF16, None) == U.ERR_UNSUPPORTED
+
+
+def test_pad_to_multiple_host():
+    """Padding to a multiple of P puts the pad positions in a document of
+    their own (host logic, CPU tensors)."""
+    import torch
+    from long_context_sequence_seq_gb300 import ulysses as U
+    x = torch.arange(2 * 10 * 3 * 2, dtype=torch.float32).reshape(2, 10, 3, 2)
+    (p,), cu, S = U.pad_to_multiple([x], 4)
+    assert S == 10 and p.shape == (2, 12, 3, 2)
+    assert torch.equal(p[:, :10], x) and torch.count_nonzero(p[:, 10:]) == 0
+    assert cu.tolist() == [0, 10, 12]
+    (q,), cu2, _ = U.pad_to_multiple([x[:1]], 4, torch.tensor([0, 4, 10], dtype=torch.int32))
+    assert cu2.tolist() == [0, 4, 10, 12]
+    (r,), cu3, _ = U.pad_to_multiple([x[:, :8]], 4)
+    assert r.shape[1] == 8 and cu3 is None
