@@ -73,6 +73,14 @@ enum { ULYSSES_BF16 = 0, ULYSSES_FP32 = 1 };
  * with D = 128 and the fp32 SIMT kernels otherwise; SIMT forces the latter. */
 enum { ULYSSES_KERNEL_AUTO = 0, ULYSSES_KERNEL_SIMT = 1 };
 
+/* Self-test of the failure path shared by every kernel: launches one CTA that
+ * waits on an mbarrier nothing arrives on, bounded by limit_ns (0 < limit_ns
+ * <= 2e9).  The wait gives up, the kernel records ULYSSES_ERR_TIMEOUT in the
+ * device error word and exits; ulysses_check then reports it and clears the
+ * word.  No GPU fault or hang is involved: the context stays usable.
+ * Returns ULYSSES_ERR_INVALID for an out-of-range limit. */
+int ulysses_selftest_wait_timeout(int64_t limit_ns, void* stream);
+
 /* ---------------------------------------------------------------------------
  * All-to-all #1 (step 3): sequence layout -> head layout of one stage.
  *   x_seq   [B][S][H][D], read only.

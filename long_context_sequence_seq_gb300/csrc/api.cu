@@ -14,6 +14,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace ulysses {
 
@@ -239,6 +240,29 @@ int noalloc_scratch(float** out) {
 }  // namespace
 
 extern "C" {
+
+// One CTA waits on an mbarrier that nothing arrives on: the bounded wait used
+// by every kernel gives up after limit_ns, records ULYSSES_ERR_TIMEOUT in the
+// device error word and the kernel exits.
+__global__ void selftest_wait_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(&bar, 1);
+    abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  tc::mbar_wait(&bar, 0, &abort_flag, limit_ns);
+}
+
+int ulysses_selftest_wait_timeout(int64_t limit_ns, void* stream) {
+  if (limit_ns <= 0 || limit_ns > (int64_t)kWaitLimitNs)
+    return set_error(ULYSSES_ERR_INVALID, "limit_ns must be in (0, %llu]", (unsigned long long)kWaitLimitNs);
+  selftest_wait_kernel<<<1, 32, 0, (cudaStream_t)stream>>>((uint64_t)limit_ns);
+  count_launch();
+  return check_launch("selftest_wait");
+}
 
 int ulysses_seq2head(const void* x_seq, void* x_head, int64_t S, int B, int H, int D, int P,
                      int head_chunk, int stage, int dtype, void* stream) {

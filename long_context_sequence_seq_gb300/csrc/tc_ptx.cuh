@@ -54,14 +54,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // give-up; callers then skip to the kernel's clean-up path.
 // A null abort_flag makes the wait ignore other threads' aborts (used to
 // drain in-flight asynchronous work before tearing down); it stays bounded.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (abort_flag != nullptr && *abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       raise_error(kErrTimeout);
       if (abort_flag != nullptr) *abort_flag = 1;
       return false;

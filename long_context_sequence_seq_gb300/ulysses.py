@@ -44,6 +44,7 @@ def lib():
     L.ulysses_seq2head.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
     L.ulysses_head2seq.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
     L.ulysses_head2seq_add.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
+    L.ulysses_selftest_wait_timeout.argtypes = [i64, vp]
     L.ulysses_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, i32,
                                    vp, i32, i32, f32, i32, vp]
     L.ulysses_attn_bwd_workspace.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32]
@@ -289,3 +290,9 @@ def set_kernel(which: int):
 
 def launch_count() -> int:
     return int(lib().ulysses_launch_count())
+
+
+def selftest_wait_timeout(limit_ns=50_000_000, stream=None):
+    """Launch the bounded-wait self-test (a wait nothing completes); the next
+    check() raises UlyssesError with code ERR_TIMEOUT."""
+    _ck(lib().ulysses_selftest_wait_timeout(int(limit_ns), _stream(stream)))

@@ -117,3 +117,10 @@ def test_pad_to_multiple_host():
     assert cu2.tolist() == [0, 4, 10, 12]
     (r,), cu3, _ = U.pad_to_multiple([x[:, :8]], 4)
     assert r.shape[1] == 8 and cu3 is None
+
+
+def test_selftest_wait_rejects_bad_limits(libpath):
+    from long_context_sequence_seq_gb300 import ulysses as U
+    L = U.lib()
+    assert L.ulysses_selftest_wait_timeout(0, None) == U.ERR_INVALID
+    assert L.ulysses_selftest_wait_timeout(3_000_000_000, None) == U.ERR_INVALID
