@@ -326,6 +326,35 @@ def e2e_measure(w, dev, cu_np, steps, warmup):
             "d2h_bytes_per_step": d2h, "ms_per_step": t * 1e3}
 
 
+def ring_measure(w, dev, steps, warmup):
+    """The ring-attention variant of the same layer (P virtual ranks, KV
+    chunks met one ring step at a time, partial results merged by LSE), timed
+    forward + backward with CUDA events on inputs resident on the device."""
+    from long_context_sequence_seq_gb300 import ulysses as U
+    if w.B != 1 or w.packed:
+        return None
+    q, k, v, do = inputs.make_seq_inputs(w, device=dev)
+
+    def step():
+        o, lse = U.ring_attention_fwd(q, k, v, w.P, causal=w.causal)
+        U.ring_attention_bwd(q, k, v, o, do, lse, w.P, causal=w.causal)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    U.check()
+    t = a.elapsed_time(b) / 1e3 / steps
+    fl = 14.0 * w.D * pairs_total(w, None) * w.H_q
+    return {"ms_per_step": t * 1e3, "tflops_fwd_bwd": fl / t / 1e12,
+            "note": "same layer as the ring variant: attention blocks of S/P tokens, LSE merges"}
+
+
 def cpu_baseline(w, cu_np, budget_s=12.0):
     """The fp64 oracle as it stands on the host cores, on a bounded sample:
     forward + backward of one (q head, kv head) pair over a causal prefix of
@@ -403,11 +432,13 @@ def gpu_arm(args):
     hbm, bf16, bf16_sus, peak_src = load_peaks()
     relay_gbs = None
     e2e = None
+    ring = None
     del step
     torch.cuda.empty_cache()
     if not args.kernels_only:
         relay_gbs, _ = measure_relayout(w, dev)
         e2e = e2e_measure(w, dev, cu_np, max(1, args.steps // 2), max(1, args.warmup // 2))
+        ring = ring_measure(w, dev, max(1, args.steps // 2), 1) if args.ring else None
     # dominant kernel = attention backward (2.5x the forward's FLOPs)
     bwd_per_launch_s = t_bwd / n_launch_attn
     achieved = fl_bwd / n_launch_attn / bwd_per_launch_s / 1e12
@@ -434,6 +465,8 @@ def gpu_arm(args):
         "clocks": clk,
         "e2e": e2e,
     }
+    if ring is not None:
+        res["ring_variant"] = ring
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, cu_np)
     if rank == 0:
@@ -487,6 +520,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="qwen3_4b_64k", choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ring", action="store_true",
+                    help="also time the ring-attention variant of the same layer")
     ap.add_argument("--kernels-only", action="store_true",
                     help="skip the isolated re-layout and end-to-end measurements (profiling runs)")
     ap.add_argument("--seq-len", type=int, default=0,

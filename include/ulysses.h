@@ -73,6 +73,26 @@ enum { ULYSSES_BF16 = 0, ULYSSES_FP32 = 1 };
  * with D = 128 and the fp32 SIMT kernels otherwise; SIMT forces the latter. */
 enum { ULYSSES_KERNEL_AUTO = 0, ULYSSES_KERNEL_SIMT = 1 };
 
+/* ---------------------------------------------------------------------------
+ * Ring-attention variant (the scheme the pages compare Ulysses with): each
+ * rank keeps its query chunk and meets the KV chunks one ring step at a time.
+ *
+ * ulysses_lse_merge folds one step's partial attention into a running result:
+ *   first != 0:  o_acc = o_part,  lse_acc = lse_part
+ *   otherwise:   LSE = log(e^{lse_acc} + e^{lse_part}),
+ *                o_acc = e^{lse_acc - LSE} o_acc + e^{lse_part - LSE} o_part,
+ *                lse_acc = LSE   (rows with no key in either stay empty)
+ *   o_acc [rows][D] fp32 and lse_acc [rows] fp32 are read and written;
+ *   o_part [rows][D] in `dtype` and lse_part [rows] fp32 are read.
+ *   D must be a multiple of 32.
+ * ulysses_cast_f32 writes n fp32 values as `dtype` (the merged O's output).
+ * ulysses_add_f32 adds n fp32 values into dst (summing the steps' dQ/dK/dV).
+ * All pointers are device pointers; asynchronous on `stream`. */
+int ulysses_lse_merge(float* o_acc, float* lse_acc, const void* o_part, const float* lse_part,
+                      int64_t rows, int D, int dtype, int first, void* stream);
+int ulysses_cast_f32(void* dst, const float* src, int64_t n, int dtype, void* stream);
+int ulysses_add_f32(float* dst, const float* src, int64_t n, void* stream);
+
 /* Self-test of the failure path shared by every kernel: launches one CTA that
  * waits on an mbarrier nothing arrives on, bounded by limit_ns (0 < limit_ns
  * <= 2e9).  The wait gives up, the kernel records ULYSSES_ERR_TIMEOUT in the

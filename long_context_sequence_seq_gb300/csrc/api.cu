@@ -264,6 +264,30 @@ int ulysses_selftest_wait_timeout(int64_t limit_ns, void* stream) {
   return check_launch("selftest_wait");
 }
 
+int ulysses_lse_merge(float* o_acc, float* lse_acc, const void* o_part, const float* lse_part,
+                      int64_t rows, int D, int dtype, int first, void* stream) {
+  if (!elt_size(dtype)) return set_error(ULYSSES_ERR_INVALID, "unknown dtype %d", dtype);
+  if (rows < 0 || D <= 0 || D % 32) return set_error(ULYSSES_ERR_INVALID, "bad sizes rows=%lld D=%d", (long long)rows, D);
+  if (rows == 0) return ULYSSES_OK;
+  if (!o_acc || !lse_acc || !o_part || !lse_part) return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  return launch_lse_merge(o_acc, lse_acc, o_part, lse_part, rows, D, dtype, first ? 1 : 0, (cudaStream_t)stream);
+}
+
+int ulysses_cast_f32(void* dst, const float* src, int64_t n, int dtype, void* stream) {
+  if (!elt_size(dtype)) return set_error(ULYSSES_ERR_INVALID, "unknown dtype %d", dtype);
+  if (n < 0) return set_error(ULYSSES_ERR_INVALID, "bad size %lld", (long long)n);
+  if (n == 0) return ULYSSES_OK;
+  if (!dst || !src) return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  return launch_cast_f32(dst, src, n, dtype, (cudaStream_t)stream);
+}
+
+int ulysses_add_f32(float* dst, const float* src, int64_t n, void* stream) {
+  if (n < 0) return set_error(ULYSSES_ERR_INVALID, "bad size %lld", (long long)n);
+  if (n == 0) return ULYSSES_OK;
+  if (!dst || !src) return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  return launch_add_f32(dst, src, n, (cudaStream_t)stream);
+}
+
 int ulysses_seq2head(const void* x_seq, void* x_head, int64_t S, int B, int H, int D, int P,
                      int head_chunk, int stage, int dtype, void* stream) {
   return relayout(true, x_seq, x_head, S, B, H, D, P, head_chunk, stage, dtype, stream);

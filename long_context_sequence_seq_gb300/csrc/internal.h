@@ -29,5 +29,9 @@ int launch_simt_fwd(const AttnArgs& a, cudaStream_t st);
 int launch_simt_bwd(const AttnArgs& a, cudaStream_t st);
 int launch_delta(const AttnArgs& a, cudaStream_t st);
 int launch_check_seqlens(const int32_t* cu, int nd, int64_t S, cudaStream_t st);
+int launch_lse_merge(float* o_acc, float* lse_acc, const void* o_part, const float* lse_part, int64_t rows,
+                     int D, int dtype, int first, cudaStream_t st);                       // ring.cu
+int launch_cast_f32(void* dst, const float* src, int64_t n, int dtype, cudaStream_t st);  // ring.cu
+int launch_add_f32(float* dst, const float* src, int64_t n, cudaStream_t st);             // ring.cu
 
 }  // namespace ulysses

@@ -45,6 +45,9 @@ def lib():
     L.ulysses_head2seq.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
     L.ulysses_head2seq_add.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
     L.ulysses_selftest_wait_timeout.argtypes = [i64, vp]
+    L.ulysses_lse_merge.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, vp]
+    L.ulysses_cast_f32.argtypes = [vp, vp, i64, i32, vp]
+    L.ulysses_add_f32.argtypes = [vp, vp, i64, vp]
     L.ulysses_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, i32,
                                    vp, i32, i32, f32, i32, vp]
     L.ulysses_attn_bwd_workspace.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32]
@@ -296,3 +299,84 @@ def selftest_wait_timeout(limit_ns=50_000_000, stream=None):
     """Launch the bounded-wait self-test (a wait nothing completes); the next
     check() raises UlyssesError with code ERR_TIMEOUT."""
     _ck(lib().ulysses_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+# --------------------------------------------------------------- ring variant
+
+def _chunks(x_seq, P):
+    """Each rank's token chunk of a [1,S,H,D] tensor in head layout [1,H,L,D]
+    (the library's re-layout with one rank over the chunk)."""
+    L = x_seq.shape[1] // P
+    return [seq2head(x_seq[:, r * L:(r + 1) * L], 1) for r in range(P)]
+
+
+def ring_attention_fwd(q_seq, k_seq, v_seq, P, causal=True, scale=None, stream=None):
+    """Ring-attention variant of the same layer (the scheme the pages compare
+    Ulysses with), on P virtual ranks: rank r keeps query chunk r and meets KV
+    chunk (r - t) mod P at ring step t; steps whose chunk lies wholly in the
+    future are skipped under the causal mask, the diagonal step is causal and
+    the others are full.  The steps' (O, LSE) are merged with their
+    log-sum-exp weights.  Returns (O [1,S,H_q,D], LSE chunks [P,H_q,L])."""
+    B, S, Hq, D = q_seq.shape
+    Hkv = k_seq.shape[2]
+    if B != 1 or S % P:
+        raise ValueError("ring variant: B == 1 and S divisible by P")
+    L, dt, st = S // P, _dtype_code(q_seq), _stream(stream)
+    qc, kc, vc = _chunks(q_seq, P), _chunks(k_seq, P), _chunks(v_seq, P)
+    out = torch.empty_like(q_seq)
+    lse = torch.empty((P, Hq, L), dtype=torch.float32, device=q_seq.device)
+    o_acc = torch.empty((Hq * L, D), dtype=torch.float32, device=q_seq.device)
+    oh = torch.empty_like(qc[0])
+    for r in range(P):
+        first = 1
+        for t in range(P):
+            c = (r - t) % P
+            if causal and c > r:
+                continue
+            op, lp = attn_fwd(qc[r], kc[c], vc[c], Hq, Hkv, 1, causal=causal and c == r, scale=scale,
+                              stream=stream)
+            _ck(lib().ulysses_lse_merge(_p(o_acc), _p(lse[r]), _p(op), _p(lp), Hq * L, D, dt, first, st))
+            first = 0
+        _ck(lib().ulysses_cast_f32(_p(oh), _p(o_acc), oh.numel(), dt, st))
+        head2seq(oh, out[:, r * L:(r + 1) * L], 1, stream=stream)
+    return out, lse
+
+
+def ring_attention_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, P, causal=True, scale=None, stream=None):
+    """Backward of ring_attention_fwd: every (query chunk, KV chunk) step runs
+    the attention backward with the merged LSE and O, and the steps' partial
+    dQ, dK, dV are summed.  Returns fp32 (dQ, dK, dV) in sequence layout."""
+    B, S, Hq, D = q_seq.shape
+    Hkv = k_seq.shape[2]
+    L, st = S // P, _stream(stream)
+    qc, kc, vc = _chunks(q_seq, P), _chunks(k_seq, P), _chunks(v_seq, P)
+    oc, doc = _chunks(o_seq, P), _chunks(do_seq, P)
+    dev = q_seq.device
+    dq_acc = [None] * P
+    dk_acc = [None] * P
+    dv_acc = [None] * P
+
+    def acc(lst, i, part):
+        if lst[i] is None:
+            lst[i] = part
+        else:
+            _ck(lib().ulysses_add_f32(_p(lst[i]), _p(part), part.numel(), st))
+
+    for r in range(P):
+        for t in range(P):
+            c = (r - t) % P
+            if causal and c > r:
+                continue
+            dqp, dkp, dvp = attn_bwd(qc[r], kc[c], vc[c], oc[r], doc[r], lse[r].unsqueeze(0), Hq, Hkv, 1,
+                                     causal=causal and c == r, scale=scale, stream=stream)
+            acc(dq_acc, r, dqp)
+            acc(dk_acc, c, dkp)
+            acc(dv_acc, c, dvp)
+    dq = torch.empty(q_seq.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(k_seq.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(v_seq.shape, dtype=torch.float32, device=dev)
+    for r in range(P):
+        head2seq(dq_acc[r], dq[:, r * L:(r + 1) * L], 1, stream=stream)
+        head2seq(dk_acc[r], dk[:, r * L:(r + 1) * L], 1, stream=stream)
+        head2seq(dv_acc[r], dv[:, r * L:(r + 1) * L], 1, stream=stream)
+    return dq, dk, dv
