@@ -355,6 +355,43 @@ def ring_measure(w, dev, steps, warmup):
             "note": "same layer as the ring variant: attention blocks of S/P tokens, LSE merges"}
 
 
+def proj_measure(w, dev, reps=10):
+    """The QKV projection with its head-layout epilogue and the output
+    projection reading O from head layout, at the workload's model width,
+    on synthetic weights (N(0, 1/fan_in)); CUDA events, median of reps."""
+    from long_context_sequence_seq_gb300 import ulysses as U
+    if not w.hidden or w.dtype != "bf16" or w.B != 1:
+        return None
+    g = torch.Generator(device=dev).manual_seed(inputs.SEED_Q + 100)
+    nf = (w.H_q + 2 * w.H_kv) * w.D
+    x = torch.randn(w.S, w.hidden, device=dev, generator=g).to(torch.bfloat16)
+    wq = (torch.randn(nf, w.hidden, device=dev, generator=g) / w.hidden ** 0.5).to(torch.bfloat16)
+    o = torch.randn(w.H_q, w.S, w.D, device=dev, generator=g).to(torch.bfloat16)
+    wo = (torch.randn(w.hidden, w.H_q * w.D, device=dev, generator=g) / (w.H_q * w.D) ** 0.5).to(torch.bfloat16)
+    qkv = torch.empty((w.H_q + 2 * w.H_kv, w.S, w.D), dtype=torch.bfloat16, device=dev)
+    y = torch.empty((w.S, w.hidden), dtype=torch.bfloat16, device=dev)
+    res = {}
+    for name, fn, fl in (("qkv_proj", lambda: U.qkv_proj(x, wq, w.H_q, w.H_kv, out=qkv), 2.0 * w.S * nf * w.hidden),
+                         ("out_proj", lambda: U.out_proj(o, wo, out=y), 2.0 * w.S * w.hidden * w.H_q * w.D)):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) / 1e3)
+        t = statistics.median(ts)
+        res[name] = {"ms": t * 1e3, "tflops": fl / t / 1e12}
+    U.check()
+    res["hidden"] = w.hidden
+    res["weights"] = "synthetic N(0, 1/fan_in)"
+    return res
+
+
 def cpu_baseline(w, cu_np, budget_s=12.0):
     """The fp64 oracle as it stands on the host cores, on a bounded sample:
     forward + backward of one (q head, kv head) pair over a causal prefix of
@@ -433,12 +470,14 @@ def gpu_arm(args):
     relay_gbs = None
     e2e = None
     ring = None
+    proj = None
     del step
     torch.cuda.empty_cache()
     if not args.kernels_only:
         relay_gbs, _ = measure_relayout(w, dev)
         e2e = e2e_measure(w, dev, cu_np, max(1, args.steps // 2), max(1, args.warmup // 2))
         ring = ring_measure(w, dev, max(1, args.steps // 2), 1) if args.ring else None
+        proj = proj_measure(w, dev) if args.proj else None
     # dominant kernel = attention backward (2.5x the forward's FLOPs)
     bwd_per_launch_s = t_bwd / n_launch_attn
     achieved = fl_bwd / n_launch_attn / bwd_per_launch_s / 1e12
@@ -467,6 +506,8 @@ def gpu_arm(args):
     }
     if ring is not None:
         res["ring_variant"] = ring
+    if proj is not None:
+        res["projections_fused_relayout"] = proj
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, cu_np)
     if rank == 0:
@@ -522,6 +563,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ring", action="store_true",
                     help="also time the ring-attention variant of the same layer")
+    ap.add_argument("--proj", action="store_true",
+                    help="also time the projections with the re-layout fused in")
     ap.add_argument("--kernels-only", action="store_true",
                     help="skip the isolated re-layout and end-to-end measurements (profiling runs)")
     ap.add_argument("--seq-len", type=int, default=0,

@@ -74,6 +74,29 @@ enum { ULYSSES_BF16 = 0, ULYSSES_FP32 = 1 };
 enum { ULYSSES_KERNEL_AUTO = 0, ULYSSES_KERNEL_SIMT = 1 };
 
 /* ---------------------------------------------------------------------------
+ * Projections with the re-layout fused in (steps 2 and 6: on one device the
+ * all-to-alls around the projections become addressing).  bf16 operands, fp32
+ * accumulation, bf16 results; tcgen05 GEMM.
+ *
+ * ulysses_qkv_proj:  [Q | K | V] = X W_qkv^T, written straight into head layout.
+ *   x         [S][hidden]                       (the tokens' hidden states)
+ *   w_qkv     [(H_q + 2 H_kv) D][hidden]        (row f = weights of output feature f;
+ *             features ordered Q heads, K heads, V heads, D per head)
+ *   qkv_head  [H_q + 2 H_kv][S][D] written: the head layout of all ranks, i.e.
+ *             what ulysses_seq2head (stage -1) gives for the projected Q, K, V.
+ *   Needs D in {64, 128}, hidden % 64 == 0, (H_q + 2 H_kv) D % 256 == 0.
+ * ulysses_out_proj:  Y = O W_o^T, reading O straight out of head layout.
+ *   o_head    [H_q][S][D]  (O_seq[s][h D + d] = o_head[h][s][d])
+ *   w_o       [hidden][H_q D]
+ *   y         [S][hidden] written.
+ *   Needs D in {64, 128}, hidden % 256 == 0.
+ * All pointers device, 16-byte aligned; asynchronous on `stream`. */
+int ulysses_qkv_proj(const void* x, const void* w_qkv, void* qkv_head, int64_t S, int hidden, int H_q,
+                     int H_kv, int D, void* stream);
+int ulysses_out_proj(const void* o_head, const void* w_o, void* y, int64_t S, int H_q, int D, int hidden,
+                     void* stream);
+
+/* ---------------------------------------------------------------------------
  * Ring-attention variant (the scheme the pages compare Ulysses with): each
  * rank keeps its query chunk and meets the KV chunks one ring step at a time.
  *

@@ -43,6 +43,7 @@ int check_launch(const char* what) {
 unsigned read_error_api(cudaStream_t st);
 unsigned read_error_attn_tc_fwd(cudaStream_t st);
 unsigned read_error_attn_tc_bwd(cudaStream_t st);
+unsigned read_error_proj_gemm(cudaStream_t st);
 ULYSSES_ERROR_READER(read_error_api)
 
 // cu_seqlens check: cu[0] == 0, cu[nd] == S, non-decreasing.
@@ -264,6 +265,32 @@ int ulysses_selftest_wait_timeout(int64_t limit_ns, void* stream) {
   return check_launch("selftest_wait");
 }
 
+int ulysses_qkv_proj(const void* x, const void* w_qkv, void* qkv_head, int64_t S, int hidden, int H_q,
+                     int H_kv, int D, void* stream) {
+  if (S < 0 || hidden <= 0 || H_q <= 0 || H_kv <= 0) return set_error(ULYSSES_ERR_INVALID, "bad sizes");
+  if (D != 64 && D != 128) return set_error(ULYSSES_ERR_UNSUPPORTED, "head dim %d not in {64,128}", D);
+  if (hidden % 64) return set_error(ULYSSES_ERR_UNSUPPORTED, "hidden=%d must be a multiple of 64", hidden);
+  if (((H_q + 2 * H_kv) * D) % 256)
+    return set_error(ULYSSES_ERR_UNSUPPORTED, "(H_q + 2 H_kv) D = %d must be a multiple of 256", (H_q + 2 * H_kv) * D);
+  if (S == 0) return ULYSSES_OK;
+  if (!x || !w_qkv || !qkv_head) return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(qkv_head))
+    return set_error(ULYSSES_ERR_INVALID, "buffers must be 16-byte aligned");
+  return launch_qkv_proj(x, w_qkv, qkv_head, S, hidden, H_q + 2 * H_kv, D, (cudaStream_t)stream);
+}
+
+int ulysses_out_proj(const void* o_head, const void* w_o, void* y, int64_t S, int H_q, int D, int hidden,
+                     void* stream) {
+  if (S < 0 || hidden <= 0 || H_q <= 0) return set_error(ULYSSES_ERR_INVALID, "bad sizes");
+  if (D != 64 && D != 128) return set_error(ULYSSES_ERR_UNSUPPORTED, "head dim %d not in {64,128}", D);
+  if (hidden % 256) return set_error(ULYSSES_ERR_UNSUPPORTED, "hidden=%d must be a multiple of 256", hidden);
+  if (S == 0) return ULYSSES_OK;
+  if (!o_head || !w_o || !y) return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  if (!aligned16(o_head) || !aligned16(w_o) || !aligned16(y))
+    return set_error(ULYSSES_ERR_INVALID, "buffers must be 16-byte aligned");
+  return launch_out_proj(o_head, w_o, y, S, H_q, D, hidden, (cudaStream_t)stream);
+}
+
 int ulysses_lse_merge(float* o_acc, float* lse_acc, const void* o_part, const float* lse_part,
                       int64_t rows, int D, int dtype, int first, void* stream) {
   if (!elt_size(dtype)) return set_error(ULYSSES_ERR_INVALID, "unknown dtype %d", dtype);
@@ -467,7 +494,8 @@ int ulysses_check(void* stream) {
   cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return set_error(ULYSSES_ERR_CUDA, "stream error: %s", cudaGetErrorString(e));
-  unsigned w = read_error_api(st) | read_error_attn_tc_fwd(st) | read_error_attn_tc_bwd(st);
+  unsigned w = read_error_api(st) | read_error_attn_tc_fwd(st) | read_error_attn_tc_bwd(st) |
+               read_error_proj_gemm(st);
   e = cudaGetLastError();
   if (e != cudaSuccess) return set_error(ULYSSES_ERR_CUDA, "error-word read failed: %s", cudaGetErrorString(e));
   if (w & kErrTimeout) return set_error(ULYSSES_ERR_TIMEOUT, "a kernel gave up a bounded wait");

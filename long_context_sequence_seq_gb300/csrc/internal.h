@@ -33,5 +33,9 @@ int launch_lse_merge(float* o_acc, float* lse_acc, const void* o_part, const flo
                      int D, int dtype, int first, cudaStream_t st);                       // ring.cu
 int launch_cast_f32(void* dst, const float* src, int64_t n, int dtype, cudaStream_t st);  // ring.cu
 int launch_add_f32(float* dst, const float* src, int64_t n, cudaStream_t st);             // ring.cu
+int launch_qkv_proj(const void* x, const void* w, void* qkv_head, int64_t S, int hidden, int n_heads, int D,
+                    cudaStream_t st);                                                     // proj_gemm.cu
+int launch_out_proj(const void* o_head, const void* w, void* y, int64_t S, int H_q, int D, int hidden,
+                    cudaStream_t st);                                                     // proj_gemm.cu
 
 }  // namespace ulysses

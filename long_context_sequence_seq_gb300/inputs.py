@@ -41,6 +41,7 @@ class Workload:
     packed: bool = False
     B: int = 1
     causal: bool = True
+    hidden: int = 0   # model width for the projection GEMMs (0: none given)
 
     @property
     def G(self) -> int:
@@ -49,8 +50,8 @@ class Workload:
 
 WORKLOADS = {
     "tiny_mha_fp32": Workload("tiny_mha_fp32", 256, 8, 8, 64, 2, 4, "fp32"),
-    "qwen3_4b_8k": Workload("qwen3_4b_8k", 8192, 32, 8, 128, 4, 8, "bf16"),
-    "qwen3_4b_64k": Workload("qwen3_4b_64k", 65536, 32, 8, 128, 4, 8, "bf16"),
+    "qwen3_4b_8k": Workload("qwen3_4b_8k", 8192, 32, 8, 128, 4, 8, "bf16", hidden=2560),
+    "qwen3_4b_64k": Workload("qwen3_4b_64k", 65536, 32, 8, 128, 4, 8, "bf16", hidden=2560),
     "llama31_8b_packed": Workload("llama31_8b_packed", 131072, 32, 8, 128, 8, 4,
                                   "bf16", packed=True),
     "million_token": Workload("million_token", 1048576, 32, 8, 128, 8, 4, "bf16"),

@@ -48,6 +48,8 @@ def lib():
     L.ulysses_lse_merge.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, vp]
     L.ulysses_cast_f32.argtypes = [vp, vp, i64, i32, vp]
     L.ulysses_add_f32.argtypes = [vp, vp, i64, vp]
+    L.ulysses_qkv_proj.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, vp]
+    L.ulysses_out_proj.argtypes = [vp, vp, vp, i64, i32, i32, i32, vp]
     L.ulysses_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, i32,
                                    vp, i32, i32, f32, i32, vp]
     L.ulysses_attn_bwd_workspace.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32]
@@ -380,3 +382,29 @@ def ring_attention_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, P, causal=True, 
         head2seq(dk_acc[r], dk[:, r * L:(r + 1) * L], 1, stream=stream)
         head2seq(dv_acc[r], dv[:, r * L:(r + 1) * L], 1, stream=stream)
     return dq, dk, dv
+
+
+
+# --------------------------------------------------------------- projections
+
+def qkv_proj(x, w_qkv, H_q, H_kv, out=None, stream=None):
+    """[Q|K|V] = X W_qkv^T written straight into head layout: x [S,hidden]
+    bf16, w_qkv [(H_q+2H_kv) D, hidden] bf16 -> [H_q+2H_kv, S, D] bf16."""
+    S, hidden = x.shape
+    nf = w_qkv.shape[0]
+    D = nf // (H_q + 2 * H_kv)
+    if out is None:
+        out = torch.empty((H_q + 2 * H_kv, S, D), dtype=torch.bfloat16, device=x.device)
+    _ck(lib().ulysses_qkv_proj(_p(x), _p(w_qkv), _p(out), S, hidden, H_q, H_kv, D, _stream(stream)))
+    return out
+
+
+def out_proj(o_head, w_o, out=None, stream=None):
+    """Y = O W_o^T with O read from head layout: o_head [H_q, S, D] bf16,
+    w_o [hidden, H_q D] bf16 -> [S, hidden] bf16."""
+    H_q, S, D = o_head.shape
+    hidden = w_o.shape[0]
+    if out is None:
+        out = torch.empty((S, hidden), dtype=torch.bfloat16, device=o_head.device)
+    _ck(lib().ulysses_out_proj(_p(o_head), _p(w_o), _p(out), S, H_q, D, hidden, _stream(stream)))
+    return out

@@ -124,3 +124,16 @@ def test_selftest_wait_rejects_bad_limits(libpath):
     L = U.lib()
     assert L.ulysses_selftest_wait_timeout(0, None) == U.ERR_INVALID
     assert L.ulysses_selftest_wait_timeout(3_000_000_000, None) == U.ERR_INVALID
+
+
+def test_projection_validation(libpath):
+    from long_context_sequence_seq_gb300 import ulysses as U
+    L = U.lib()
+    d = ctypes.c_void_p(256)
+    # hidden not a multiple of 64 / features not a multiple of 256 / D unsupported
+    assert L.ulysses_qkv_proj(d, d, d, 128, 100, 4, 2, 128, None) == U.ERR_UNSUPPORTED
+    assert L.ulysses_qkv_proj(d, d, d, 128, 256, 3, 1, 64, None) == U.ERR_UNSUPPORTED
+    assert L.ulysses_qkv_proj(d, d, d, 128, 256, 4, 2, 96, None) == U.ERR_UNSUPPORTED
+    assert L.ulysses_out_proj(d, d, d, 128, 4, 128, 300, None) == U.ERR_UNSUPPORTED
+    # empty input: a no-op
+    assert L.ulysses_out_proj(d, d, d, 0, 4, 128, 256, None) == U.OK
