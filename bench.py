@@ -392,6 +392,42 @@ def proj_measure(w, dev, reps=10):
     return res
 
 
+def fused_measure(w, dev, cu_np, steps, warmup):
+    """The same layer step with the all-to-alls folded into the attention
+    kernels (no re-layout launches, no head-layout copies), inputs resident on
+    the device, CUDA events around the whole step."""
+    from long_context_sequence_seq_gb300 import ulysses as U
+    if w.B != 1 or w.dtype != "bf16" or w.D != 128:
+        return None
+    q, k, v, do = inputs.make_seq_inputs(w, device=dev)
+    cu = None if cu_np is None else torch.from_numpy(cu_np).to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H_q, w.S), dtype=torch.float32, device=dev)
+    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+    nb = U.lib().ulysses_layer_fused_workspace(w.S, w.B, w.H_q, w.H_kv, w.D, w.P, w.head_chunk, U.BF16)
+    ws = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+
+    def step():
+        U.layer_fwd_fused(q, k, v, w.P, w.head_chunk, cu, w.causal, out=o, lse=lse)
+        U.layer_bwd_fused(q, k, v, o, do, lse, w.P, w.head_chunk, cu, w.causal, workspace=ws, dq=dq, dk=dk, dv=dv)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    U.check()
+    t = a.elapsed_time(b) / 1e3 / steps
+    return {"ms_per_step": t * 1e3, "tokens_per_s": w.B * w.S / t,
+            "note": "all-to-alls folded into the attention kernels' addressing"}
+
+
 def cpu_baseline(w, cu_np, budget_s=12.0):
     """The fp64 oracle as it stands on the host cores, on a bounded sample:
     forward + backward of one (q head, kv head) pair over a causal prefix of
@@ -471,6 +507,7 @@ def gpu_arm(args):
     e2e = None
     ring = None
     proj = None
+    fused = None
     del step
     torch.cuda.empty_cache()
     if not args.kernels_only:
@@ -478,6 +515,7 @@ def gpu_arm(args):
         e2e = e2e_measure(w, dev, cu_np, max(1, args.steps // 2), max(1, args.warmup // 2))
         ring = ring_measure(w, dev, max(1, args.steps // 2), 1) if args.ring else None
         proj = proj_measure(w, dev) if args.proj else None
+        fused = fused_measure(w, dev, cu_np, max(1, args.steps // 2), 1) if args.fused else None
     # dominant kernel = attention backward (2.5x the forward's FLOPs)
     bwd_per_launch_s = t_bwd / n_launch_attn
     achieved = fl_bwd / n_launch_attn / bwd_per_launch_s / 1e12
@@ -508,6 +546,8 @@ def gpu_arm(args):
         res["ring_variant"] = ring
     if proj is not None:
         res["projections_fused_relayout"] = proj
+    if fused is not None:
+        res["fused_relayout_step"] = fused
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, cu_np)
     if rank == 0:
@@ -565,6 +605,8 @@ def main():
                     help="also time the ring-attention variant of the same layer")
     ap.add_argument("--proj", action="store_true",
                     help="also time the projections with the re-layout fused in")
+    ap.add_argument("--fused", action="store_true",
+                    help="also time the layer step with the all-to-alls folded into the attention kernels")
     ap.add_argument("--kernels-only", action="store_true",
                     help="skip the isolated re-layout and end-to-end measurements (profiling runs)")
     ap.add_argument("--seq-len", type=int, default=0,

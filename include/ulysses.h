@@ -74,6 +74,29 @@ enum { ULYSSES_BF16 = 0, ULYSSES_FP32 = 1 };
 enum { ULYSSES_KERNEL_AUTO = 0, ULYSSES_KERNEL_SIMT = 1 };
 
 /* ---------------------------------------------------------------------------
+ * The layer with the all-to-alls folded into the attention kernels: on one
+ * device the head view of the sequence layout is a strided view, so the
+ * kernels read Q/K/V/O/dO through sequence-layout TMA tensor maps and write
+ * O, dQ (tensor reduce-adds), dK and dV straight into the sequence layout; no
+ * head-layout copies and no re-layout launches.  Arguments and results as
+ * ulysses_layer_fwd / ulysses_layer_bwd (same UPipe stage loop), restricted to
+ * B == 1, bf16, S >= 128, D = 128 for the backward (64 or 128 forward), and no
+ * kv-head replication; otherwise ULYSSES_ERR_UNSUPPORTED.  The backward's
+ * workspace (ulysses_layer_fused_workspace bytes) holds the stage's D_i terms.
+ * Results equal the unfused layer's (dQ up to the order of its fp32 additions). */
+size_t ulysses_layer_fused_workspace(int64_t S, int B, int H_q, int H_kv, int D, int P, int head_chunk,
+                                     int dtype);
+int ulysses_layer_fwd_fused(const void* q_seq, const void* k_seq, const void* v_seq, void* o_seq, float* lse,
+                            int64_t S, int B, int H_q, int H_kv, int D, int P, int head_chunk,
+                            const int32_t* cu_seqlens, int num_docs, int causal, float scale, int dtype,
+                            void* stream);
+int ulysses_layer_bwd_fused(const void* q_seq, const void* k_seq, const void* v_seq, const void* o_seq,
+                            const void* do_seq, const float* lse, float* dq_seq, float* dk_seq, float* dv_seq,
+                            int64_t S, int B, int H_q, int H_kv, int D, int P, int head_chunk,
+                            const int32_t* cu_seqlens, int num_docs, int causal, float scale, int dtype,
+                            void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
  * Projections with the re-layout fused in (steps 2 and 6: on one device the
  * all-to-alls around the projections become addressing).  bf16 operands, fp32
  * accumulation, bf16 results; tcgen05 GEMM.

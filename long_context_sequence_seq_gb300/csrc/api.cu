@@ -265,6 +265,99 @@ int ulysses_selftest_wait_timeout(int64_t limit_ns, void* stream) {
   return check_launch("selftest_wait");
 }
 
+// ---------------------------------------------------------------------------
+// The layer with the all-to-alls folded into the attention kernels'
+// addressing (sequence-layout tensor maps and stores): no head-layout copies.
+static int fused_check(AttnArgs& a, int B, int H_kv, int P, bool bwd) {
+  if (B != 1) return set_error(ULYSSES_ERR_UNSUPPORTED, "fused layer: B must be 1");
+  if (H_kv < P) return set_error(ULYSSES_ERR_UNSUPPORTED, "fused layer: kv-head replication not supported");
+  if (a.dtype != ULYSSES_BF16 || (bwd && a.D != 128) || a.S < 128)
+    return set_error(ULYSSES_ERR_UNSUPPORTED, "fused layer: bf16, S >= 128%s", bwd ? ", D = 128" : "");
+  return ULYSSES_OK;
+}
+
+size_t ulysses_layer_fused_workspace(int64_t S, int B, int H_q, int H_kv, int D, int P, int head_chunk,
+                                     int dtype) {
+  AttnArgs a;
+  if (attn_shape(a, S, B, H_q, H_kv, D, P, head_chunk, 0, nullptr, 0, 1, 0.f, dtype)) return 0;
+  return align256(delta_bytes(S, B, a.nq));
+}
+
+int ulysses_layer_fwd_fused(const void* q_seq, const void* k_seq, const void* v_seq, void* o_seq, float* lse,
+                            int64_t S, int B, int H_q, int H_kv, int D, int P, int head_chunk,
+                            const int32_t* cu_seqlens, int num_docs, int causal, float scale, int dtype,
+                            void* stream) {
+  AttnArgs a;
+  int rc = attn_shape(a, S, B, H_q, H_kv, D, P, head_chunk, 0, cu_seqlens, num_docs, causal, scale, dtype);
+  if (rc) return rc;
+  if (S == 0) return ULYSSES_OK;
+  if ((rc = fused_check(a, B, H_kv, P, false))) return rc;
+  if (!q_seq || !k_seq || !v_seq || !o_seq || !lse) return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  if (!aligned16(q_seq) || !aligned16(k_seq) || !aligned16(v_seq) || !aligned16(o_seq))
+    return set_error(ULYSSES_ERR_INVALID, "buffers must be 16-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  const int C = a.nq, stages = P * (H_q / P / C);
+  const size_t e = (size_t)D * 2;   // bytes per head of a row
+  if (cu_seqlens) { rc = launch_check_seqlens(cu_seqlens, num_docs, S, st); if (rc) return rc; }
+  for (int s = 0; s < stages; ++s) {
+    int n = 0, h0 = 0;
+    stage_span(H_q, P, C, s, &n, &h0);
+    AttnArgs sa = a;
+    sa.seq = 1; sa.hq_tot = H_q; sa.hkv_tot = H_kv;
+    sa.q = (const char*)q_seq + h0 * e;
+    sa.k = (const char*)k_seq + (h0 / a.G) * e;
+    sa.v = (const char*)v_seq + (h0 / a.G) * e;
+    sa.o_out = (char*)o_seq + h0 * e;
+    sa.lse = lse + (size_t)h0 * S;
+    sa.lse_bstride = (int64_t)H_q * S;
+    if ((rc = launch_tc_fwd(sa, st))) return rc;
+  }
+  return ULYSSES_OK;
+}
+
+int ulysses_layer_bwd_fused(const void* q_seq, const void* k_seq, const void* v_seq, const void* o_seq,
+                            const void* do_seq, const float* lse, float* dq_seq, float* dk_seq, float* dv_seq,
+                            int64_t S, int B, int H_q, int H_kv, int D, int P, int head_chunk,
+                            const int32_t* cu_seqlens, int num_docs, int causal, float scale, int dtype,
+                            void* workspace, size_t ws_bytes, void* stream) {
+  AttnArgs a;
+  int rc = attn_shape(a, S, B, H_q, H_kv, D, P, head_chunk, 0, cu_seqlens, num_docs, causal, scale, dtype);
+  if (rc) return rc;
+  if (S == 0) return ULYSSES_OK;
+  if ((rc = fused_check(a, B, H_kv, P, true))) return rc;
+  if (!q_seq || !k_seq || !v_seq || !o_seq || !do_seq || !lse || !dq_seq || !dk_seq || !dv_seq || !workspace)
+    return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  if (!aligned16(q_seq) || !aligned16(k_seq) || !aligned16(v_seq) || !aligned16(o_seq) || !aligned16(do_seq) ||
+      !aligned16(dq_seq) || !aligned16(dk_seq) || !aligned16(dv_seq))
+    return set_error(ULYSSES_ERR_INVALID, "buffers must be 16-byte aligned");
+  if (ws_bytes < delta_bytes(S, B, a.nq))
+    return set_error(ULYSSES_ERR_INVALID, "workspace too small: %zu < %zu", ws_bytes, delta_bytes(S, B, a.nq));
+  cudaStream_t st = (cudaStream_t)stream;
+  const int C = a.nq, stages = P * (H_q / P / C);
+  const size_t e = (size_t)D * 2, ef = (size_t)D;   // bf16 bytes / fp32 elements per head of a row
+  if (cu_seqlens) { rc = launch_check_seqlens(cu_seqlens, num_docs, S, st); if (rc) return rc; }
+  for (int s = 0; s < stages; ++s) {
+    int n = 0, h0 = 0;
+    stage_span(H_q, P, C, s, &n, &h0);
+    const int kh0 = h0 / a.G;
+    AttnArgs sa = a;
+    sa.seq = 1; sa.hq_tot = H_q; sa.hkv_tot = H_kv;
+    sa.q = (const char*)q_seq + h0 * e;
+    sa.k = (const char*)k_seq + kh0 * e;
+    sa.v = (const char*)v_seq + kh0 * e;
+    sa.o = (const char*)o_seq + h0 * e;
+    sa.dO = (const char*)do_seq + h0 * e;
+    sa.lse_in = lse + (size_t)h0 * S;
+    sa.lse_bstride = (int64_t)H_q * S;
+    sa.dq = dq_seq + h0 * ef;
+    sa.dk = dk_seq + kh0 * ef;
+    sa.dv = dv_seq + kh0 * ef;
+    sa.delta = (float*)workspace;
+    if ((rc = launch_tc_bwd(sa, st))) return rc;
+  }
+  return ULYSSES_OK;
+}
+
 int ulysses_qkv_proj(const void* x, const void* w_qkv, void* qkv_head, int64_t S, int hidden, int H_q,
                      int H_kv, int D, void* stream) {
   if (S < 0 || hidden <= 0 || H_q <= 0 || H_kv <= 0) return set_error(ULYSSES_ERR_INVALID, "bad sizes");

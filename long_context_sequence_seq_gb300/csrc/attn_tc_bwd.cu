@@ -96,10 +96,13 @@ struct BwdLayout {
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
                                                       float* __restrict__ delta,
-                                                      float* __restrict__ dq, int64_t rows) {
+                                                      float* __restrict__ dq, int64_t rows, int64_t S,
+                                                      int seq, int hq_tot) {
   const int lane = threadIdx.x & 31;
-  const int64_t row = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (row >= rows) return;
+  const int64_t hr = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;   // head-major row
+  if (hr >= rows) return;
+  // where the row lives: head layout [n][S][D], or sequence layout [S][hq_tot][D]
+  const int64_t row = seq ? (hr % S) * hq_tot + hr / S : hr;
   // 128 features = 32 lanes x 4
   const uint2 ov = *reinterpret_cast<const uint2*>(o + row * D + lane * 4);
   const uint2 dv = *reinterpret_cast<const uint2*>(dO + row * D + lane * 4);
@@ -114,7 +117,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-  if (lane == 0) delta[row] = s;
+  if (lane == 0) delta[hr] = s;
   *reinterpret_cast<float4*>(dq + row * D + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
@@ -133,7 +136,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const float* __restrict__ lse, const float* __restrict__ delta,
                   float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
                   int64_t S, int nq, int G, int64_t lse_bstride, const int32_t* __restrict__ cu,
-                  int nd, int causal, float scale) {
+                  int nd, int causal, float scale, const __grid_constant__ CUtensorMap tmDQ, int seq,
+                  int hkv_tot) {
   using L = BwdLayout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -210,8 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       mbar_expect_tx(kv_full, 2 * L::kTileKV);
       for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(sK + c * L::kChunkKV, &tmK, c * 64, (int)k0, kvh, kv_full);
-        tma_load_3d(sV + c * L::kChunkKV, &tmV, c * 64, (int)k0, kvh, kv_full);
+        // head layout: (feature, row, head); sequence layout: (feature, head, row)
+        tma_load_3d(sK + c * L::kChunkKV, &tmK, c * 64, seq ? kvh : (int)k0, seq ? (int)k0 : kvh, kv_full);
+        tma_load_3d(sV + c * L::kChunkKV, &tmV, c * 64, seq ? kvh : (int)k0, seq ? (int)k0 : kvh, kv_full);
       }
       for (int it = 0; it < n_it; ++it) {
         const int st = it % NSTAGE;
@@ -221,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q0 = (int)(q_lo + (int64_t)(it % n_qb) * BMQ);
         mbar_expect_tx(&q_full[st], 2 * L::kTileQ);
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(sQ + st * L::kTileQ + c * L::kChunkQ, &tmQ, c * 64, q0, n, &q_full[st]);
-          tma_load_3d(sDO + st * L::kTileQ + c * L::kChunkQ, &tmDO, c * 64, q0, n, &q_full[st]);
+          tma_load_3d(sQ + st * L::kTileQ + c * L::kChunkQ, &tmQ, c * 64, seq ? n : q0, seq ? q0 : n, &q_full[st]);
+          tma_load_3d(sDO + st * L::kTileQ + c * L::kChunkQ, &tmDO, c * 64, seq ? n : q0, seq ? q0 : n, &q_full[st]);
         }
       }
     }
@@ -326,10 +331,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = kvh * G + x / n_qb;
         const int64_t q0 = q_lo + (int64_t)(x % n_qb) * BMQ;
         const int64_t rows = S - q0 < BMQ ? S - q0 : BMQ;
-        float* dst = dq + ((int64_t)n * S + q0) * D;
-        const int64_t r0 = rows < 32 ? rows : 32;
-        if (r0 > 0) bulk_reduce_add_f32(dst, sQ + st * L::kTileQ, (uint32_t)(r0 * D * 4));
-        if (rows > 32) bulk_reduce_add_f32(dst + 32 * D, sDO + st * L::kTileQ, (uint32_t)((rows - 32) * D * 4));
+        if (seq) {
+          // rows of one head are H_q D apart in the sequence layout: tensor
+          // reduce-adds of 32-row boxes (rows past S are dropped)
+          tma_reduce_add_3d(&tmDQ, sQ + st * L::kTileQ, 0, n, (int)q0);
+          if (rows > 32) tma_reduce_add_3d(&tmDQ, sDO + st * L::kTileQ, 0, n, (int)q0 + 32);
+        } else {
+          float* dst = dq + ((int64_t)n * S + q0) * D;
+          const int64_t r0 = rows < 32 ? rows : 32;
+          if (r0 > 0) bulk_reduce_add_f32(dst, sQ + st * L::kTileQ, (uint32_t)(r0 * D * 4));
+          if (rows > 32) bulk_reduce_add_f32(dst + 32 * D, sDO + st * L::kTileQ, (uint32_t)((rows - 32) * D * 4));
+        }
         bulk_commit();
         bulk_wait_read0();
         mbar_arrive(&q_empty[st]);
@@ -455,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue: half 0 writes dV, half 1 writes scale * dK of this key block
     if (ok && n_it > 0 && mbar_wait_warp(fin, 0, abort_flag)) {
       tc_fence_after();
-      float* dst = (h == 0 ? dv : dk) + ((int64_t)kvh * S + j) * D;
+      float* dst = (h == 0 ? dv : dk) + (seq ? (int64_t)j * hkv_tot + kvh : (int64_t)kvh * S + j) * D;
       const float mul = h == 0 ? 1.f : scale;
       const uint32_t col0 = h == 0 ? kColDV : kColDK;
 #pragma unroll 1
@@ -474,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (n_it == 0 && j < S) {
       // no query sees these keys: zero gradients
-      float* dst = (h == 0 ? dv : dk) + ((int64_t)kvh * S + j) * D;
+      float* dst = (h == 0 ? dv : dk) + (seq ? (int64_t)j * hkv_tot + kvh : (int64_t)kvh * S + j) * D;
       for (int c = 0; c < D; c += 4) *reinterpret_cast<float4*>(dst + c) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
@@ -496,16 +508,25 @@ bool tc_bwd_supported(const AttnArgs& a) {
 int launch_tc_bwd(const AttnArgs& a, cudaStream_t st) {
   const int64_t rows = (int64_t)a.n_q * a.S;
   bwd_pre_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(
-      (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, a.delta, a.dq, rows);
+      (const __nv_bfloat16*)a.o, (const __nv_bfloat16*)a.dO, a.delta, a.dq, rows, a.S, a.seq, a.hq_tot);
   count_launch();
   int rc = check_launch("bwd_pre");
   if (rc) return rc;
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdq;
   const int n_kv = a.n_q / a.G;
-  if ((rc = make_tmap_bf16_3d(&tq, a.q, a.S, a.n_q, D, BMQ))) return rc;
-  if ((rc = make_tmap_bf16_3d(&tdo, a.dO, a.S, a.n_q, D, BMQ))) return rc;
-  if ((rc = make_tmap_bf16_3d(&tk, a.k, a.S, n_kv, D, BN))) return rc;
-  if ((rc = make_tmap_bf16_3d(&tv, a.v, a.S, n_kv, D, BN))) return rc;
+  if (a.seq) {
+    if ((rc = make_tmap_bf16_seq(&tq, a.q, a.S, a.n_q, a.hq_tot, D, BMQ))) return rc;
+    if ((rc = make_tmap_bf16_seq(&tdo, a.dO, a.S, a.n_q, a.hq_tot, D, BMQ))) return rc;
+    if ((rc = make_tmap_bf16_seq(&tk, a.k, a.S, n_kv, a.hkv_tot, D, BN))) return rc;
+    if ((rc = make_tmap_bf16_seq(&tv, a.v, a.S, n_kv, a.hkv_tot, D, BN))) return rc;
+    if ((rc = make_tmap_f32_seq(&tdq, a.dq, a.S, a.n_q, a.hq_tot, D, 32))) return rc;
+  } else {
+    if ((rc = make_tmap_bf16_3d(&tq, a.q, a.S, a.n_q, D, BMQ))) return rc;
+    if ((rc = make_tmap_bf16_3d(&tdo, a.dO, a.S, a.n_q, D, BMQ))) return rc;
+    if ((rc = make_tmap_bf16_3d(&tk, a.k, a.S, n_kv, D, BN))) return rc;
+    if ((rc = make_tmap_bf16_3d(&tv, a.v, a.S, n_kv, D, BN))) return rc;
+    tdq = tq;   // not read in the head layout
+  }
   const int smem = BwdLayout::kAlloc;
   static bool attr_set = false;
   if (!attr_set) {
@@ -515,7 +536,7 @@ int launch_tc_bwd(const AttnArgs& a, cudaStream_t st) {
   dim3 grid((unsigned)n_kv, (unsigned)((a.S + BN - 1) / BN));
   tc_bwd_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, a.lse_in, a.delta, a.dq, a.dk, a.dv,
                                               a.S, a.nq, a.G, a.lse_bstride, a.cu, a.nd, a.causal,
-                                              a.scale);
+                                              a.scale, tdq, a.seq, a.hkv_tot);
   count_launch();
   return check_launch("tc_bwd");
 }

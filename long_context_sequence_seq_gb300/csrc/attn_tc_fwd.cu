@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out,
                   float* __restrict__ lse, int64_t S, int nq, int G, int64_t lse_bstride,
-                  const int32_t* __restrict__ cu, int nd, int causal, float sl2) {
+                  const int32_t* __restrict__ cu, int nd, int causal, float sl2, int seq, int hq_tot) {
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -137,7 +137,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       mbar_expect_tx(q_full, L::kTileQ);
-      for (int c = 0; c < D / 64; ++c) tma_load_3d(sQ + c * L::kChunkQ, &tmQ, c * 64, (int)q0, n, q_full);
+      // head layout: (feature, row, head); sequence layout: (feature, head, row)
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(sQ + c * L::kChunkQ, &tmQ, c * 64, seq ? n : (int)q0, seq ? (int)q0 : n, q_full);
       // K tiles into the K ring (slot freed by QK_j), V tiles into the V ring
       // (freed by PV_j); K runs one tile ahead: K0 K1 V0 K2 V1 ...
       bool go = true;
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int k0 = (int)(kv_lo + (int64_t)j * BN);
           uint8_t* dst = sKV + (kv * NRING + r) * L::kTileKV;
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(dst + c * L::kChunkKV, kv ? &tmV : &tmK, c * 64, k0, kvh, full);
+            tma_load_3d(dst + c * L::kChunkKV, kv ? &tmV : &tmK, c * 64, seq ? kvh : k0, seq ? k0 : kvh, full);
         }
     }
     __syncwarp();
@@ -321,7 +323,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait();
         reg_fence(ov);
         if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)n * S + i) * D + c * 32);
+          const int64_t row = seq ? (int64_t)i * hq_tot + n : (int64_t)n * S + i;
+          uint4* dst = reinterpret_cast<uint4*>(out + row * D + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             uint4 w;
@@ -351,9 +354,15 @@ int launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   CUtensorMap tq, tk, tv;
   const int n_kv = a.n_q / a.G;
   int rc;
-  if ((rc = make_tmap_bf16_3d(&tq, a.q, a.S, a.n_q, D, BM))) return rc;
-  if ((rc = make_tmap_bf16_3d(&tk, a.k, a.S, n_kv, D, BN))) return rc;
-  if ((rc = make_tmap_bf16_3d(&tv, a.v, a.S, n_kv, D, BN))) return rc;
+  if (a.seq) {
+    if ((rc = make_tmap_bf16_seq(&tq, a.q, a.S, a.n_q, a.hq_tot, D, BM))) return rc;
+    if ((rc = make_tmap_bf16_seq(&tk, a.k, a.S, n_kv, a.hkv_tot, D, BN))) return rc;
+    if ((rc = make_tmap_bf16_seq(&tv, a.v, a.S, n_kv, a.hkv_tot, D, BN))) return rc;
+  } else {
+    if ((rc = make_tmap_bf16_3d(&tq, a.q, a.S, a.n_q, D, BM))) return rc;
+    if ((rc = make_tmap_bf16_3d(&tk, a.k, a.S, n_kv, D, BN))) return rc;
+    if ((rc = make_tmap_bf16_3d(&tv, a.v, a.S, n_kv, D, BN))) return rc;
+  }
   const int smem = FwdLayout<D>::kAlloc;
   static bool attr_set = false;
   if (!attr_set) {
@@ -364,7 +373,7 @@ int launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   dim3 grid((unsigned)a.n_q, (unsigned)n_qt);
   tc_fwd_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, (__nv_bfloat16*)a.o_out, a.lse, a.S,
                                                  a.nq, a.G, a.lse_bstride, a.cu, a.nd, a.causal,
-                                                 a.scale * kLog2e);
+                                                 a.scale * kLog2e, a.seq, a.hq_tot);
   count_launch();
   return check_launch("tc_fwd");
 }

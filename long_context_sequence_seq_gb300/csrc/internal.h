@@ -21,6 +21,10 @@ struct AttnArgs {
   int G; int D;
   int64_t lse_bstride;  // LSE element stride between batch entries
   const int32_t* cu; int nd; int causal; float scale; int dtype;
+  // seq != 0: q/k/v/o/dO and dq/dk/dv point at the stage's first head inside
+  // sequence-layout tensors [S][hq_tot or hkv_tot][D] (B == 1) instead of
+  // head-layout buffers: the re-layout is folded into the kernels' addressing
+  int seq; int hq_tot; int hkv_tot;
 };
 
 int launch_relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, int D,

@@ -113,6 +113,17 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssr
       "r"(smem_u32(ssrc)), "r"(bytes)
       : "memory");
 }
+// Tiled tensor reduce-add (fp32 map) of a shared-memory box into global
+// memory through a 3D tensor map; out-of-range elements of the box are
+// dropped.  Coordinates must not be negative.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* ssrc, int x, int y,
+                                                  int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(ssrc)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the issuing thread's bulk groups have finished READING shared memory.
 __device__ __forceinline__ void bulk_wait_read0() {
@@ -346,5 +357,11 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // Host: encode a 3D bf16 tensor map over [heads][S][D] with box {64, rows, 1}
 // and 128-byte swizzle.  Implemented in tmap.cu.
 int make_tmap_bf16_3d(CUtensorMap* map, const void* base, int64_t S, int heads, int D, int rows);
+// Sequence-layout views: `heads` consecutive heads of rows holding row_heads
+// heads each ([S][row_heads][D] in memory, base at the first head): dims
+// (D, heads, S), box {64, 1, rows} bf16 (coordinates: feature, head, row) and,
+// for fp32 reductions, box {D, 1, rows}.
+int make_tmap_bf16_seq(CUtensorMap* map, const void* base, int64_t S, int heads, int row_heads, int D, int rows);
+int make_tmap_f32_seq(CUtensorMap* map, const void* base, int64_t S, int heads, int row_heads, int D, int rows);
 
 }  // namespace ulysses

@@ -50,6 +50,12 @@ def lib():
     L.ulysses_add_f32.argtypes = [vp, vp, i64, vp]
     L.ulysses_qkv_proj.argtypes = [vp, vp, vp, i64, i32, i32, i32, i32, vp]
     L.ulysses_out_proj.argtypes = [vp, vp, vp, i64, i32, i32, i32, vp]
+    L.ulysses_layer_fused_workspace.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32]
+    L.ulysses_layer_fused_workspace.restype = ctypes.c_size_t
+    L.ulysses_layer_fwd_fused.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, vp, i32,
+                                          i32, ctypes.c_float, i32, vp]
+    L.ulysses_layer_bwd_fused.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32,
+                                          i32, vp, i32, i32, ctypes.c_float, i32, vp, ctypes.c_size_t, vp]
     L.ulysses_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, i32, i32,
                                    vp, i32, i32, f32, i32, vp]
     L.ulysses_attn_bwd_workspace.argtypes = [i64, i32, i32, i32, i32, i32, i32, i32, i32]
@@ -408,3 +414,42 @@ def out_proj(o_head, w_o, out=None, stream=None):
         out = torch.empty((S, hidden), dtype=torch.bfloat16, device=o_head.device)
     _ck(lib().ulysses_out_proj(_p(o_head), _p(w_o), _p(out), S, H_q, D, hidden, _stream(stream)))
     return out
+
+
+# --------------------------------------------------------------- fused layer
+
+def layer_fwd_fused(q_seq, k_seq, v_seq, P, head_chunk, cu_seqlens=None, causal=True, scale=None,
+                    out=None, lse=None, stream=None):
+    """layer_fwd with the all-to-alls folded into the kernels' addressing (no
+    head-layout copies): returns (O [1,S,H_q,D], LSE [1,H_q,S])."""
+    B, S, H_q, D = q_seq.shape
+    H_kv = k_seq.shape[2]
+    out = torch.empty_like(q_seq) if out is None else out
+    lse = torch.empty((B, H_q, S), dtype=torch.float32, device=q_seq.device) if lse is None else lse
+    cp, nd = _cu(cu_seqlens)
+    _ck(lib().ulysses_layer_fwd_fused(_p(q_seq), _p(k_seq), _p(v_seq), _p(out), _p(lse), S, B, H_q, H_kv, D, P,
+                                      head_chunk, cp, nd, int(bool(causal)), float(scale or 0.0),
+                                      _dtype_code(q_seq), _stream(stream)))
+    return out, lse
+
+
+def layer_bwd_fused(q_seq, k_seq, v_seq, o_seq, do_seq, lse, P, head_chunk, cu_seqlens=None, causal=True,
+                    scale=None, workspace=None, dq=None, dk=None, dv=None, stream=None):
+    """layer_bwd with the all-to-alls folded into the kernels' addressing:
+    returns fp32 (dQ, dK, dV) in sequence layout."""
+    B, S, H_q, D = q_seq.shape
+    H_kv = k_seq.shape[2]
+    dt = _dtype_code(q_seq)
+    dev = q_seq.device
+    if workspace is None:
+        nb = lib().ulysses_layer_fused_workspace(S, B, H_q, H_kv, D, P, head_chunk, dt)
+        workspace = torch.empty(max(nb, 256), dtype=torch.uint8, device=dev)
+    dq = torch.empty(q_seq.shape, dtype=torch.float32, device=dev) if dq is None else dq
+    dk = torch.empty(k_seq.shape, dtype=torch.float32, device=dev) if dk is None else dk
+    dv = torch.empty(v_seq.shape, dtype=torch.float32, device=dev) if dv is None else dv
+    cp, nd = _cu(cu_seqlens)
+    _ck(lib().ulysses_layer_bwd_fused(_p(q_seq), _p(k_seq), _p(v_seq), _p(o_seq), _p(do_seq), _p(lse), _p(dq),
+                                      _p(dk), _p(dv), S, B, H_q, H_kv, D, P, head_chunk, cp, nd,
+                                      int(bool(causal)), float(scale or 0.0), dt, _p(workspace),
+                                      workspace.numel(), _stream(stream)))
+    return dq, dk, dv

@@ -137,3 +137,15 @@ def test_projection_validation(libpath):
     assert L.ulysses_out_proj(d, d, d, 128, 4, 128, 300, None) == U.ERR_UNSUPPORTED
     # empty input: a no-op
     assert L.ulysses_out_proj(d, d, d, 0, 4, 128, 256, None) == U.OK
+
+
+def test_fused_layer_validation(libpath):
+    from long_context_sequence_seq_gb300 import ulysses as U
+    L = U.lib()
+    d = ctypes.c_void_p(256)
+    args = [d] * 5
+    # B > 1, fp32 and kv-head replication are outside the fused layer
+    assert L.ulysses_layer_fwd_fused(*args, 256, 2, 8, 8, 128, 2, 4, None, 0, 1, 0.0, U.BF16, None) == U.ERR_UNSUPPORTED
+    assert L.ulysses_layer_fwd_fused(*args, 256, 1, 8, 8, 128, 2, 4, None, 0, 1, 0.0, U.FP32, None) == U.ERR_UNSUPPORTED
+    assert L.ulysses_layer_fwd_fused(*args, 256, 1, 8, 2, 128, 4, 2, None, 0, 1, 0.0, U.BF16, None) == U.ERR_UNSUPPORTED
+    assert U.lib().ulysses_layer_fused_workspace(4096, 1, 32, 8, 128, 4, 8, U.BF16) == 8 * 4096 * 4
