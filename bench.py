@@ -257,15 +257,16 @@ def e2e_measure(w, dev, cu_np, steps, warmup):
     from long_context_sequence_seq_gb300 import ulysses as U
     dt = torch.bfloat16 if w.dtype == "bf16" else torch.float32
     hq, hk, hv, hdo = (t.cpu().pin_memory() for t in inputs.make_seq_inputs(w, device=dev, small_on_host=False))
-    q, k, v, do = (torch.empty(t.shape, dtype=dt, device=dev) for t in (hq, hk, hv, hdo))
+    # two device copies of the inputs: step i+1's upload runs under step i
+    bufs = [[torch.empty(t.shape, dtype=dt, device=dev) for t in (hq, hk, hv, hdo)] for _ in range(2)]
     ws = U.layer_workspace(w.S, w.B, w.H_q, w.H_kv, w.D, w.P, w.head_chunk,
                            U.BF16 if w.dtype == "bf16" else U.FP32, dev)
     cu = None if cu_np is None else torch.from_numpy(cu_np).to(dev)
-    o = torch.empty_like(q)
+    o = torch.empty(hq.shape, dtype=dt, device=dev)
     lse = torch.empty((w.B, w.H_q, w.S), dtype=torch.float32, device=dev)
-    dq = torch.empty(q.shape, dtype=torch.float32, device=dev)
-    dk = torch.empty(k.shape, dtype=torch.float32, device=dev)
-    dv = torch.empty(v.shape, dtype=torch.float32, device=dev)
+    dq = torch.empty(hq.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(hk.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(hv.shape, dtype=torch.float32, device=dev)
     ho = torch.empty(o.shape, dtype=dt).pin_memory()
     hdq = torch.empty(dq.shape, dtype=torch.float32).pin_memory()
     hdk = torch.empty(dk.shape, dtype=torch.float32).pin_memory()
@@ -273,51 +274,68 @@ def e2e_measure(w, dev, cu_np, steps, warmup):
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv))
 
-    # Copies run on a second stream where the data allows: dO is uploaded
-    # under the forward, O is downloaded under the backward, and a step's
-    # dQ/dK/dV download overlaps the next step's Q/K/V upload (the two copy
-    # directions use separate engines).  Events order every buffer reuse.
+    # Copies run on two side streams, one per direction (separate copy
+    # engines): step i's inputs are uploaded into buffer set i % 2 while step
+    # i-1 computes from the other set; O is downloaded under the backward and
+    # dQ/dK/dV under the next step's forward.  Events order every reuse of a
+    # buffer, so every step still moves all of its inputs and results.
     main = torch.cuda.current_stream(dev)
-    cs = torch.cuda.Stream(device=dev)
-    ev = {name: torch.cuda.Event() for name in ("do_in", "fwd", "o_out", "bwd", "g_out")}
-    state = {"first": True}
+    up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]        # set j uploaded
+    ev_used = [torch.cuda.Event() for _ in range(2)]      # set j no longer read
+    ev = {name: torch.cuda.Event() for name in ("fwd", "o_out", "bwd", "g_out")}
+    state = {"i": 0}
 
-    def step():
-        for d_, h_ in ((q, hq), (k, hk), (v, hv)):
-            d_.copy_(h_, non_blocking=True)
-        cs.wait_stream(main)                      # the previous backward read dO
-        with torch.cuda.stream(cs):
-            do.copy_(hdo, non_blocking=True)
-            ev["do_in"].record(cs)
-        if not state["first"]:
+    def upload(i):
+        j = i % 2
+        if i >= 2:
+            up.wait_event(ev_used[j])
+        with torch.cuda.stream(up):
+            for d_, h_ in zip(bufs[j], (hq, hk, hv, hdo)):
+                d_.copy_(h_, non_blocking=True)
+            ev_in[j].record(up)
+
+    def step(last):
+        i = state["i"]
+        j = i % 2
+        q, k, v, do = bufs[j]
+        main.wait_event(ev_in[j])
+        if i > 0:
             main.wait_event(ev["o_out"])          # O of the previous step is on the host
         U.layer_fwd(q, k, v, w.P, w.head_chunk, cu, w.causal, workspace=ws, out=o, lse=lse)
         ev["fwd"].record(main)
-        with torch.cuda.stream(cs):
-            cs.wait_event(ev["fwd"])
+        with torch.cuda.stream(down):
+            down.wait_event(ev["fwd"])
             ho.copy_(o, non_blocking=True)
-            ev["o_out"].record(cs)
-        main.wait_event(ev["do_in"])
-        if not state["first"]:
+            ev["o_out"].record(down)
+        if not last:
+            upload(i + 1)                         # the next step's inputs, under this step
+        if i > 0:
             main.wait_event(ev["g_out"])          # the previous gradients are on the host
         U.layer_bwd(q, k, v, o, do, lse, w.P, w.head_chunk, cu, w.causal, workspace=ws,
                     dq=dq, dk=dk, dv=dv)
+        ev_used[j].record(main)
         ev["bwd"].record(main)
-        with torch.cuda.stream(cs):
-            cs.wait_event(ev["bwd"])
+        with torch.cuda.stream(down):
+            down.wait_event(ev["bwd"])
             for h_, d_ in ((hdq, dq), (hdk, dk), (hdv, dv)):
                 h_.copy_(d_, non_blocking=True)
-            ev["g_out"].record(cs)
-        state["first"] = False
+            ev["g_out"].record(down)
+        state["i"] = i + 1
 
-    for _ in range(warmup):
-        step()
+    def run(n):
+        state["i"] = 0
+        upload(0)
+        for s_ in range(n):
+            step(s_ == n - 1)
+        main.wait_event(ev["g_out"])              # the last step's results are on the host
+
+    run(warmup)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(main)
-    for _ in range(steps):
-        step()
-    main.wait_event(ev["g_out"])                  # the last step's results are on the host
+    up.wait_stream(main)
+    run(steps)                                    # the first upload is inside the timed region
     b.record(main)
     torch.cuda.synchronize()
     U.check()
@@ -512,7 +530,7 @@ def gpu_arm(args):
     torch.cuda.empty_cache()
     if not args.kernels_only:
         relay_gbs, _ = measure_relayout(w, dev)
-        e2e = e2e_measure(w, dev, cu_np, max(1, args.steps // 2), max(1, args.warmup // 2))
+        e2e = e2e_measure(w, dev, cu_np, max(1, args.steps), max(1, args.warmup // 2))
         ring = ring_measure(w, dev, max(1, args.steps // 2), 1) if args.ring else None
         proj = proj_measure(w, dev) if args.proj else None
         fused = fused_measure(w, dev, cu_np, max(1, args.steps // 2), 1) if args.fused else None
