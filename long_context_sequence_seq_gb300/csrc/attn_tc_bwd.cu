@@ -86,8 +86,8 @@ struct BwdLayout {
   static constexpr int kStat = kDS + kTileDS;                 // NSTAGE x {LSE2[64], D[64]}
   static constexpr int kBar = kStat + NSTAGE * 2 * BMQ * 4;
   // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[2], ds_full[2], dsm_free,
-  // dq_full[2], dq_empty, fin, drain, stg_full[NSTAGE]
-  static constexpr int kNumBar = 1 + 3 * NSTAGE + 7 + 3;
+  // dq_full[2], dq_empty, fin, drain, stg_full[NSTAGE], dk_done[NSTAGE]
+  static constexpr int kNumBar = 1 + 4 * NSTAGE + 7 + 3;
   static constexpr int kMisc = kBar + kNumBar * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -126,10 +126,14 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
 //                                                   readout of dQ^T_{it-1}, which
 //                                                   lived in S buffer b')
 //   wait ds_full[b]  (gradient warps finished tile it)
-//   dV += P^T_it dO_it, dK += dS^T_it Q_it, dQ^T_it = K^T dS^T_it  (into S buffer b)
-//   -> dq_full[b], dsm_free
+//   dV += P^T_it dO_it, dQ^T_it = K^T dS^T_it (into S buffer b) -> dq_full[b], dsm_free
+//   dK += dS^T_it Q_it                                             -> dk_done[stage]
 // so the tensor pipe runs tile it's gradient MMAs and tile it+1's score MMAs
-// while the gradient warps work on tile it+1.
+// while the gradient warps work on tile it+1.  dQ^T goes before dK so that its
+// readout (which frees S buffer b for the scores of it+2) overlaps dK; the
+// readout then waits for dk_done before it reuses the tile's Q buffer.  The
+// per-stage dk_done barrier cannot run two phases ahead of the readout: dK of
+// the stage's next tile needs the stage refilled, which needs this readout.
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -160,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* fin = dq_empty + 1;
   uint64_t* drain = fin + 1;
   uint64_t* stg_full = drain + 1;     // dQ tile of a stage written to its Q/dO buffers
+  uint64_t* dk_done = stg_full + NSTAGE;   // dK of a stage's tile done: its Q buffer is free
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -173,6 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&q_full[s], 2);
       mbar_init(&q_empty[s], 1);
       mbar_init(&stg_full[s], kReadWarps);
+      mbar_init(&dk_done[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -297,14 +303,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dod = sdesc_sw128(smem_u32(sDO + st * L::kTileQ), L::kChunkQ, 1024);
         const uint64_t qd = sdesc_sw128(smem_u32(sQ + st * L::kTileQ), L::kChunkQ, 1024);
         const uint64_t dsd = sdesc_sw128(smem_u32(sDS), 8192, 1024);
-        // dV and dK are independent: interleave per K step
+        // dV first (it reads P^T from S buffer b), then dQ^T into S buffer b, then
+        // dK: the dQ^T readout overlaps dK, so the next scores into buffer b
+        // wait less.
 #pragma unroll
-        for (int kk = 0; kk < BMQ / 16; ++kk) {
+        for (int kk = 0; kk < BMQ / 16; ++kk)
           mma_ts_w(tbase + kColDV, tbase + kColS + b * BMQ + packed_col(kk), sdesc_add(dod, kk * 2048), id_g,
                    (it > 0 || kk > 0) ? 1u : 0u);
-          mma_ts_w(tbase + kColDK, tbase + kColDP + b * BMQ + packed_col(kk), sdesc_add(qd, kk * 2048), id_g,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-        }
         // dQ^T = K^T dS^T into S buffer b: A = K (MN-major, 64-feature chunks
         // L::kChunkKV apart), B = dS^T ([key][query] rows of 128 B); 16 keys per step.
 #pragma unroll
@@ -313,6 +318,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                    kk > 0 ? 1u : 0u);
         mma_commit_w(&dq_full[b]);
         mma_commit_w(dsm_free);
+#pragma unroll
+        for (int kk = 0; kk < BMQ / 16; ++kk)
+          mma_ts_w(tbase + kColDK, tbase + kColDP + b * BMQ + packed_col(kk), sdesc_add(qd, kk * 2048), id_g,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_w(&dk_done[st]);
       }
       __syncwarp();
     }
@@ -375,11 +385,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(dq_empty);
       float* c0 = reinterpret_cast<float*>(sQ + sx * L::kTileQ) + d;
       float* c1 = reinterpret_cast<float*>(sDO + sx * L::kTileQ) + d;
+      // queries 32-63 into the dO buffer (dV, which read it, is done) ...
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        c0[c * D] = __uint_as_float(r0[c]) * scale;
-        c1[c * D] = __uint_as_float(r1[c]) * scale;
-      }
+      for (int c = 0; c < 32; ++c) c1[c * D] = __uint_as_float(r1[c]) * scale;
+      // ... queries 0-31 into the Q buffer once dK has read it
+      if (!mbar_wait_warp(&dk_done[sx], (x / NSTAGE) & 1, abort_flag)) break;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) c0[c * D] = __uint_as_float(r0[c]) * scale;
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&stg_full[sx]);
