@@ -290,21 +290,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
 #pragma unroll
       for (int c = 0; c < BN / 64; ++c) tmem_st32(sbuf + c * 32, pk[c]);
-      if (j > 0) {
-        // O must hold PV_{j-1} before it is rescaled for tile j
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        // O must hold PV_{j-1} before this warp rescales its rows.  A warp
+        // that keeps its max does not touch O and need not wait: PV_j comes
+        // after PV_{j-1} in issue order, and PV_j waits for every warp's P_j.
+        // The wait cannot alias an older phase: PV_{j-1+NRING} needs this
+        // warp's P for tile j-1+NRING.
         if (!mbar_wait_warp(&v_empty[(j - 1) % NRING], ((j - 1) / NRING) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld32(tbase + lane_off + kColO + c * 32, ov);
-            tmem_ld_wait();
-            reg_fence(ov);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(tbase + lane_off + kColO + c * 32, ov);
+          tmem_ld_wait();
+          reg_fence(ov);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            tmem_st32(tbase + lane_off + kColO + c * 32, ov);
-          }
+          for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+          tmem_st32(tbase + lane_off + kColO + c * 32, ov);
         }
       }
       tmem_st_wait();

@@ -73,12 +73,18 @@ def test_attention_small(S, Hq, Hkv, D, P, C, dtype, docs, causal):
     assert max_err(f64(dq), rq) <= tol
     assert max_err(f64(dk), rk) <= tol
     assert max_err(f64(dv), rv) <= tol
-    # the native layer driver gives bit-identical results
+    # the native layer driver gives bit-identical O, LSE, dK and dV.  The
+    # bf16 backward sums dQ with fp32 reduce-adds from every key block in the
+    # order they reach L2, so two runs may differ in the last bits of dQ.
     lo, ll = U.layer_fwd(q, k, v, P, C, cu_seqlens=cu, causal=causal)
     lq, lk, lv = U.layer_bwd(q, k, v, lo, do, ll, P, C, cu_seqlens=cu, causal=causal)
     U.check()
-    for a, b in ((lo, o), (ll, lse), (lq, dq), (lk, dk), (lv, dv)):
+    for a, b in ((lo, o), (ll, lse), (lk, dk), (lv, dv)):
         assert torch.equal(a, b)
+    if dtype == "fp32":
+        assert torch.equal(lq, dq)
+    else:
+        assert float((lq - dq).abs().max()) <= 1e-5 * max(1.0, float(dq.abs().max()))
 
 
 def test_tiny_mha_fp32_workload_all_chunks():
