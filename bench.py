@@ -38,7 +38,7 @@ UNIT = "tokens/s"
 # DRAM bytes per launch of the dominant kernel from an ncu capture of this
 # workload (profiles/traffic_qwen3_4b_64k.md), valid only for the kernel
 # source it was taken on (sha256 prefix); any other source reports null.
-TRAFFIC = {"qwen3_4b_64k": ("attn_tc_bwd.cu", "90ea2190f3cae3aa", 3257412864)}
+TRAFFIC = {"qwen3_4b_64k": ("attn_tc_bwd.cu", "dd46b95b04e1b9d8", 3259014912)}
 
 
 def measured_traffic(workload):

@@ -348,9 +348,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (rows > 32) tma_reduce_add_3d(&tmDQ, sDO + st * L::kTileQ, 0, n, (int)q0 + 32);
         } else {
           float* dst = dq + ((int64_t)n * S + q0) * D;
-          const int64_t r0 = rows < 32 ? rows : 32;
-          if (r0 > 0) bulk_reduce_add_f32(dst, sQ + st * L::kTileQ, (uint32_t)(r0 * D * 4));
-          if (rows > 32) bulk_reduce_add_f32(dst + 32 * D, sDO + st * L::kTileQ, (uint32_t)((rows - 32) * D * 4));
+          // 8-row (4 KB) pieces: with more, smaller reductions in flight the
+          // tile's dQ reaches L2 sooner than as two 16 KB pieces (measured)
+#pragma unroll 1
+          for (int r0 = 0; r0 < rows; r0 += 8) {
+            const int64_t nr = rows - r0 < 8 ? rows - r0 : 8;
+            const uint8_t* src = (r0 < 32 ? sQ : sDO) + st * L::kTileQ + (r0 & 31) * D * 4;
+            bulk_reduce_add_f32(dst + (int64_t)r0 * D, src, (uint32_t)(nr * D * 4));
+          }
         }
         bulk_commit();
         bulk_wait_read0();
