@@ -12,11 +12,27 @@
 #include <cstdio>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ptx.cuh"
 
 namespace ulysses {
+
+// One NVTX range per UPipe stage of the layer drivers, so a profiler that
+// records NVTX (ncu --nvtx) can attribute kernels to stages; without an
+// attached tool the push and pop are no-ops.
+struct StageRange {
+  StageRange(const char* what, int s) {
+    char name[48];
+    snprintf(name, sizeof(name), "ulysses %s stage %d", what, s);
+    nvtxRangePushA(name);
+  }
+  ~StageRange() { nvtxRangePop(); }
+  StageRange(const StageRange&) = delete;
+  StageRange& operator=(const StageRange&) = delete;
+};
 
 static thread_local char g_msg[512];
 static std::atomic<long long> g_launches{0};
@@ -300,6 +316,7 @@ int ulysses_layer_fwd_fused(const void* q_seq, const void* k_seq, const void* v_
   const size_t e = (size_t)D * 2;   // bytes per head of a row
   if (cu_seqlens) { rc = launch_check_seqlens(cu_seqlens, num_docs, S, st); if (rc) return rc; }
   for (int s = 0; s < stages; ++s) {
+    StageRange range("fused fwd", s);
     int n = 0, h0 = 0;
     stage_span(H_q, P, C, s, &n, &h0);
     AttnArgs sa = a;
@@ -337,6 +354,7 @@ int ulysses_layer_bwd_fused(const void* q_seq, const void* k_seq, const void* v_
   const size_t e = (size_t)D * 2, ef = (size_t)D;   // bf16 bytes / fp32 elements per head of a row
   if (cu_seqlens) { rc = launch_check_seqlens(cu_seqlens, num_docs, S, st); if (rc) return rc; }
   for (int s = 0; s < stages; ++s) {
+    StageRange range("fused bwd", s);
     int n = 0, h0 = 0;
     stage_span(H_q, P, C, s, &n, &h0);
     const int kh0 = h0 / a.G;
@@ -521,6 +539,7 @@ int ulysses_layer_fwd(const void* q_seq, const void* k_seq, const void* v_seq, v
   const int stages = P * (H_q / P / C);
   if (cu_seqlens) { rc = launch_check_seqlens(cu_seqlens, num_docs, S, st); if (rc) return rc; }
   for (int s = 0; s < stages; ++s) {
+    StageRange range("fwd", s);
     int n = 0, h0 = 0;
     stage_span(H_q, P, C, s, &n, &h0);
     const int ks = kv_stage(H_kv, P, s, stages);
@@ -558,6 +577,7 @@ int ulysses_layer_bwd(const void* q_seq, const void* k_seq, const void* v_seq, c
   const int stages = P * (H_q / P / C);
   if (cu_seqlens) { rc = launch_check_seqlens(cu_seqlens, num_docs, S, st); if (rc) return rc; }
   for (int s = 0; s < stages; ++s) {
+    StageRange range("bwd", s);
     int n = 0, h0 = 0;
     stage_span(H_q, P, C, s, &n, &h0);
     const int ks = kv_stage(H_kv, P, s, stages);
