@@ -43,6 +43,13 @@ What it computes, and where that is defined:
 
   with dK/dV summed over the G q heads that share a kv head.
 
+* Projections, steps 2 and 6 of the same section: every rank projects its own
+  token chunk to Q, K and V (a plain matmul with the weights, rows
+  independent), the first all-to-all then moves the projected heads; after
+  the second all-to-all every rank applies the output projection to its own
+  chunk.  Weight rows are ordered Q heads, K heads, V heads, D per head (the
+  usual fused QKV weight; the pages give no order).
+
 Readings where the pages are silent: scale 1/sqrt(D) unless given; causal
 means j <= i (diagonal included); LSE is the natural log.
 """
@@ -56,7 +63,7 @@ __all__ = [
     "stage_heads", "seq2head", "head2seq", "seq2head_bruteforce", "head2seq_bruteforce",
     "relayout_bytes_per_rank", "key_ranges", "attn_fwd", "attn_bwd",
     "attn_fwd_bruteforce", "attn_bwd_bruteforce", "ulysses_attention",
-    "ulysses_attention_bwd", "attn_rows", "attn_kv_tail", "num_pairs",
+    "ulysses_attention_bwd", "attn_rows", "attn_kv_tail", "num_pairs", "qkv_proj", "out_proj",
 ]
 
 
@@ -478,3 +485,55 @@ def attn_kv_tail(q_heads, k_g, v_g, do_heads, j0, cu_seqlens=None, causal=True, 
             dV[j[sel] - j0] += Pm[:, sel].T @ dd
             dK[j[sel] - j0] += sc * (dS[:, sel].T @ qq)
     return dK, dV
+
+
+# ----------------------------------------------------------------------------
+# Projections around the all-to-alls (steps 2 and 6)
+# ----------------------------------------------------------------------------
+
+def qkv_proj(x, w_qkv, H_q, H_kv, P=1):
+    """Step 2 then all-to-all #1: x [S, hidden], w_qkv [(H_q + 2 H_kv) D, hidden].
+
+    Rank r projects its chunk of S/P tokens, y_r = x_r w_qkv^T, viewed as
+    [S/P, H_q + 2 H_kv, D]; the chunks stacked in rank order are the sequence
+    layout of Q, K and V, and seq2head (all heads) of each gives its head
+    layout.  Returns [H_q + 2 H_kv, S, D] fp64: the Q heads, then the K heads,
+    then the V heads.
+    """
+    x, w = _as64(x), _as64(w_qkv)
+    S, hidden = x.shape
+    n_heads = H_q + 2 * H_kv
+    if w.shape[0] % n_heads or w.shape[1] != hidden:
+        raise ValueError("w_qkv must be [(H_q + 2 H_kv) D, hidden]")
+    D = w.shape[0] // n_heads
+    if S % P:
+        raise ValueError("S must be divisible by the number of ranks")
+    Sp = S // P
+    y_seq = np.zeros((1, S, n_heads, D))
+    for r in range(P):
+        y_seq[0, r * Sp:(r + 1) * Sp] = (x[r * Sp:(r + 1) * Sp] @ w.T).reshape(Sp, n_heads, D)
+    q_seq, k_seq, v_seq = y_seq[:, :, :H_q], y_seq[:, :, H_q:H_q + H_kv], y_seq[:, :, H_q + H_kv:]
+    return np.concatenate([seq2head(t, P)[0] for t in (q_seq, k_seq, v_seq)])
+
+
+def out_proj(o_head, w_o, P=1):
+    """All-to-all #2 then step 6: o_head [H_q, S, D] (every head, every
+    position), w_o [hidden, H_q D].
+
+    head2seq returns each rank its chunk with all heads, [S/P, H_q, D], which
+    is flattened to [S/P, H_q D] and projected, y_r = o_r w_o^T.  Returns
+    [S, hidden] fp64.
+    """
+    o, w = _as64(o_head), _as64(w_o)
+    Hq, S, D = o.shape
+    if w.shape[1] != Hq * D:
+        raise ValueError("w_o must be [hidden, H_q D]")
+    if S % P:
+        raise ValueError("S must be divisible by the number of ranks")
+    o_seq = np.zeros((1, S, Hq, D))
+    head2seq(o[None], o_seq, P)
+    Sp = S // P
+    y = np.zeros((S, w.shape[0]))
+    for r in range(P):
+        y[r * Sp:(r + 1) * Sp] = o_seq[0, r * Sp:(r + 1) * Sp].reshape(Sp, Hq * D) @ w.T
+    return y

@@ -474,3 +474,111 @@ def test_mutants_are_caught(monkeypatch):
     with pytest.raises(AssertionError):
         test_golden_relayout()
     monkeypatch.setattr(O, "seq2head", real_s2h)
+
+
+# ---------------------------------------------------------------- projections (steps 2 and 6)
+
+def test_golden_projections():
+    g = json.load(open(os.path.join(GOLD, "proj_2tok.json")))
+    for case in g["cases"]:
+        x = np.array(case["x"], dtype=np.float64)
+        w = np.array(case["w_qkv"], dtype=np.float64)
+        got = O.qkv_proj(x, w, case["H_q"], case["H_kv"], case["P"])
+        np.testing.assert_array_equal(got, np.array(case["qkv_head"], dtype=np.float64), err_msg=case["name"])
+        y = O.out_proj(np.array(case["o_head"], dtype=np.float64), np.array(case["w_o"], dtype=np.float64),
+                       case["P"])
+        np.testing.assert_array_equal(y, np.array(case["y"], dtype=np.float64), err_msg=case["name"])
+
+
+def _qkv_bruteforce(x, w, n_heads, D):
+    S, hidden = x.shape
+    out = np.zeros((n_heads, S, D))
+    for h in range(n_heads):
+        for s in range(S):
+            for d in range(D):
+                acc = 0.0
+                for c in range(hidden):
+                    acc += x[s, c] * w[h * D + d, c]
+                out[h, s, d] = acc
+    return out
+
+
+def _out_bruteforce(o, w):
+    Hq, S, D = o.shape
+    hidden = w.shape[0]
+    y = np.zeros((S, hidden))
+    for s in range(S):
+        for c in range(hidden):
+            acc = 0.0
+            for h in range(Hq):
+                for d in range(D):
+                    acc += o[h, s, d] * w[c, h * D + d]
+            y[s, c] = acc
+    return y
+
+
+@pytest.mark.parametrize("S,hidden,Hq,Hkv,D,P", [(8, 6, 4, 2, 3, 2), (12, 5, 3, 3, 2, 3), (4, 4, 4, 4, 4, 4)])
+def test_projections_bruteforce_and_rank_split(S, hidden, Hq, Hkv, D, P):
+    x = _rand((S, hidden), 70)
+    w = _rand(((Hq + 2 * Hkv) * D, hidden), 71)
+    got = O.qkv_proj(x, w, Hq, Hkv, P)
+    np.testing.assert_allclose(got, _qkv_bruteforce(x, w, Hq + 2 * Hkv, D), rtol=0, atol=1e-12)
+    # the rank split of the tokens does not change the result
+    np.testing.assert_allclose(O.qkv_proj(x, w, Hq, Hkv, 1), got, rtol=0, atol=1e-12)
+    o = _rand((Hq, S, D), 72)
+    wo = _rand((hidden, Hq * D), 73)
+    y = O.out_proj(o, wo, P)
+    np.testing.assert_allclose(y, _out_bruteforce(o, wo), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(O.out_proj(o, wo, 1), y, rtol=0, atol=1e-12)
+
+
+def test_projection_identity_round_trip():
+    """With hidden = H_q D and identity weights, step 2's Q heads are the
+    all-to-all of x itself, and step 6 with identity weights gives x back:
+    the two layout maps are inverse to each other."""
+    S, Hq, Hkv, D, P = 8, 4, 2, 3, 2
+    hidden = Hq * D
+    x = _rand((S, hidden), 74)
+    w = np.zeros(((Hq + 2 * Hkv) * D, hidden))
+    w[:hidden] = np.eye(hidden)
+    qkv = O.qkv_proj(x, w, Hq, Hkv, P)
+    np.testing.assert_array_equal(qkv[:Hq], O.seq2head(x.reshape(1, S, Hq, D), P)[0])
+    assert not np.any(qkv[Hq:])
+    np.testing.assert_array_equal(O.out_proj(qkv[:Hq], np.eye(hidden), P), x)
+
+
+def test_projection_mutants_are_caught():
+    """A transposed head/feature order or swapped K/V blocks in a copy of the
+    projection fail the brute-force pin."""
+    S, hidden, Hq, Hkv, D = 6, 5, 2, 1, 3
+    x = _rand((S, hidden), 75)
+    w = _rand(((Hq + 2 * Hkv) * D, hidden), 76)
+    ref = _qkv_bruteforce(x, w, Hq + 2 * Hkv, D)
+    y = x @ w.T
+    feature_major = y.reshape(S, D, Hq + 2 * Hkv).transpose(2, 0, 1)     # d-major instead of head-major
+    kv_swapped = np.concatenate([ref[:Hq], ref[Hq + Hkv:], ref[Hq:Hq + Hkv]])
+    for bad in (feature_major, kv_swapped):
+        assert np.max(np.abs(bad - ref)) > 1e-3
+
+
+def test_oracle_pool_runs_the_oracle_unchanged():
+    """The spawn pool used by the full-size GPU checks returns exactly what a
+    direct call of the oracle returns (same functions, same inputs)."""
+    from tests import oracle_pool
+    S, D = 96, 8
+    q, k, v, do = (_rand((S, D), 80 + i).astype(np.float32) for i in range(4))
+    cu = np.array([0, 40, 96])
+    (o, lse, dq, dk, dv), = oracle_pool.run(oracle_pool.head_fwd_bwd, [(q, k, v, do, cu, True)])
+    ro, rl = O.attn_fwd(q[None], k[None], v[None], cu, True)
+    rq, rk, rv = O.attn_bwd(q[None], k[None], v[None], do[None], cu, True)
+    for a, b in ((o, ro[0]), (lse, rl[0]), (dq, rq[0]), (dk, rk[0]), (dv, rv[0])):
+        np.testing.assert_array_equal(a, b)
+    rows = np.array([0, 39, 40, 95])
+    got = oracle_pool.run(oracle_pool.head_rows, [(q[rows], k, v, do[rows], rows, cu, True)])[0]
+    want = O.attn_rows(q[rows], k, v, do[rows], rows, cu, True)
+    for a, b in zip(got, want):
+        np.testing.assert_array_equal(a, b)
+    j0 = 64
+    tk, tv = oracle_pool.run(oracle_pool.head_kv_tail, [(q[j0:], k, v, do[j0:], j0, cu, True, 16)])[0]
+    np.testing.assert_allclose(tk, rk[0, j0:], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(tv, rv[0, j0:], rtol=0, atol=1e-12)
