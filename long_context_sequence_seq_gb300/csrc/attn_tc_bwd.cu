@@ -545,11 +545,8 @@ int launch_tc_bwd(const AttnArgs& a, cudaStream_t st) {
     tdq = tq;   // not read in the head layout
   }
   const int smem = BwdLayout::kAlloc;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(tc_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attr_set = true;
-  }
+  static PerDeviceOnce<> smem_once;
+  if ((rc = opt_in_smem(smem_once, (const void*)tc_bwd_kernel, smem, "tc_bwd"))) return rc;
   dim3 grid((unsigned)n_kv, (unsigned)((a.S + BN - 1) / BN));
   tc_bwd_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, a.lse_in, a.delta, a.dq, a.dk, a.dv,
                                               a.S, a.nq, a.G, a.lse_bstride, a.cu, a.nd, a.causal,

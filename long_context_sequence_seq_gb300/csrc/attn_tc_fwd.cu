@@ -366,11 +366,8 @@ int launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
     if ((rc = make_tmap_bf16_3d(&tv, a.v, a.S, n_kv, D, BN))) return rc;
   }
   const int smem = FwdLayout<D>::kAlloc;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(tc_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attr_set = true;
-  }
+  static PerDeviceOnce<> smem_once;   // one per head dim (template instance)
+  if ((rc = opt_in_smem(smem_once, (const void*)tc_fwd_kernel<D>, smem, "tc_fwd"))) return rc;
   const int64_t n_qt = (a.S + BM - 1) / BM;
   dim3 grid((unsigned)a.n_q, (unsigned)n_qt);
   tc_fwd_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, (__nv_bfloat16*)a.o_out, a.lse, a.S,

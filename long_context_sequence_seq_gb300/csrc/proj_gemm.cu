@@ -196,11 +196,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 int launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, void* out, int64_t M, int N, int K, int a_head_dim,
                 int c_head_dim, cudaStream_t st) {
   const int smem = GemmLayout::kAlloc;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    attr_set = true;
-  }
+  static PerDeviceOnce<> smem_once;
+  int rc = opt_in_smem(smem_once, (const void*)tc_gemm_kernel, smem, "tc_gemm");
+  if (rc) return rc;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
