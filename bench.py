@@ -1,9 +1,9 @@
 """Benchmark: one Ulysses attention layer step (fwd + bwd) on the GPU.
 
-A step is one pass of the whole hot path over one batch of synthetic input:
-for every virtual rank and UPipe chunk, seq2head of Q/K/V, attention forward,
-head2seq of O; then seq2head of O/dO (plus Q/K/V again), attention backward,
-head2seq of dQ/dK/dV.  Default workload: the Qwen3-4B-shaped layer at S=65536
+A step is one pass of the whole hot path over one batch of synthetic input,
+in a layer's order: for every virtual rank and UPipe chunk, seq2head of
+Q/K/V, attention forward, head2seq of O; then for every stage again seq2head
+of Q/K/V/O/dO, attention backward, head2seq of dQ/dK/dV.  Default workload: the Qwen3-4B-shaped layer at S=65536
 (H_q=32, H_kv=8, D=128, P=4 virtual ranks, head_chunk=8, bf16 N(0,1) inputs).
 
 Prints one JSON line.  `value` is tokens/s of the whole step with inputs
@@ -35,9 +35,14 @@ from long_context_sequence_seq_gb300 import inputs  # noqa: E402
 METRIC = "causal attn fwd+bwd tokens/s & TFLOPS at S=64K (% BF16 peak); re-layout GB/s"
 UNIT = "tokens/s"
 
+# Nominal dense GB300 figures (bf16 tensor, HBM3e), reported beside the
+# measured peaks for context.
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_HBM_GBS = 7900.0
+
 # DRAM bytes per launch of the dominant kernel from an ncu capture of this
-# workload (profiles/traffic_qwen3_4b_64k.md), valid only for the kernel
-# source it was taken on (sha256 prefix); any other source reports null.
+# workload, valid only for the kernel source it was taken on (sha256 prefix);
+# any other source reports null.
 TRAFFIC = {"qwen3_4b_64k": ("attn_tc_bwd.cu", "dd46b95b04e1b9d8", 3259014912)}
 
 
@@ -147,8 +152,13 @@ class ClockSampler:
 class LayerStep:
     """Device-resident buffers and the per-stage C-ABI call sequence of one step.
 
-    Attention calls are bracketed by CUDA events on the launching stream so
-    the dominant kernels' average durations come from the timed region itself.
+    The step does what a layer does: the forward over every UPipe stage, then
+    the backward over every stage, which gathers the stage's Q, K, V, O and
+    dO again (dO only exists after the whole forward).  Per stage each
+    direction is one batched gather, the attention call and one batched
+    scatter, the same launches as the native layer drivers.  CUDA events on
+    the launching stream bracket every launch group, so the attention and
+    re-layout durations come from the timed region itself.
     """
 
     def __init__(self, w, dev, cu_np):
@@ -171,61 +181,96 @@ class LayerStep:
         self.kh, self.vh = mk(C // G, dt), mk(C // G, dt)
         self.dqh = mk(C, torch.float32)
         self.dkh, self.dvh = mk(C // G, torch.float32), mk(C // G, torch.float32)
-        self.lseh = torch.empty((B, C, S), dtype=torch.float32, device=dev)
+        # B > 1: a stage's LSE rows are not contiguous in [B, H_q, S]; keep one
+        # [B, C, S] buffer per stage (the backward reads it after every forward)
+        self.stages = w.P * (w.H_q // w.P // C)
+        self.lse_st = [] if B == 1 else [torch.empty((B, C, S), dtype=torch.float32, device=dev)
+                                         for _ in range(self.stages)]
         wsb = U.attn_bwd_workspace_bytes(S, B, w.H_q, w.H_kv, D, w.P, C, 0,
                                          U.BF16 if w.dtype == "bf16" else U.FP32)
         self.ws = torch.empty(max(wsb, 256), dtype=torch.uint8, device=dev)
-        self.stages = w.P * (w.H_q // w.P // C)
-        self.events = []
+        self.events = []      # per timed step: lists of (r0, r1, r2, r3) for fwd and bwd stages
+
+    def _lse_stage(self, st):
+        w = self.w
+        hq = w.H_q // w.P
+        r, c = divmod(st, hq // w.head_chunk)
+        h0 = r * hq + c * w.head_chunk
+        # B == 1: the stage's rows of the global [B, H_q, S] LSE are contiguous
+        return self.lse[:, h0:h0 + w.head_chunk] if w.B == 1 else self.lse_st[st]
 
     def run(self, timed=False):
         U, w = self.U, self.w
-        C, G = w.head_chunk, w.G
-        ev = []
-        hq = w.H_q // w.P
+        C, G, P = w.head_chunk, w.G, w.P
+        ev_f, ev_b = [], []
+
+        def marks():
+            if not timed:
+                return None
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            return e
+
         for st in range(self.stages):
-            r, c = divmod(st, hq // C)
-            h0 = r * hq + c * C
-            # B == 1: the stage's rows of the global [B, H_q, S] LSE are contiguous
-            lse_st = self.lse[:, h0:h0 + C] if w.B == 1 else self.lseh
-            U.seq2head(self.q, w.P, C, st, out=self.qh)
-            U.seq2head(self.k, w.P, C // G, st, out=self.kh)
-            U.seq2head(self.v, w.P, C // G, st, out=self.vh)
-            e0 = torch.cuda.Event(enable_timing=True) if timed else None
-            e1 = torch.cuda.Event(enable_timing=True) if timed else None
-            if timed:
-                e0.record()
-            U.attn_fwd(self.qh, self.kh, self.vh, w.H_q, w.H_kv, w.P, C, st, self.cu, w.causal,
-                       out=self.oh, lse=lse_st)
-            if timed:
-                e1.record()
-            U.head2seq(self.oh, self.o, w.P, C, st)
-            U.seq2head(self.do, w.P, C, st, out=self.doh)
-            e2 = torch.cuda.Event(enable_timing=True) if timed else None
-            e3 = torch.cuda.Event(enable_timing=True) if timed else None
-            if timed:
-                e2.record()
-            U.attn_bwd(self.qh, self.kh, self.vh, self.oh, self.doh, lse_st, w.H_q, w.H_kv,
-                       w.P, C, st, self.cu, w.causal, workspace=self.ws, dq=self.dqh,
+            e = marks()
+            if e:
+                e[0].record()
+            U.seq2head_n([(self.q, self.qh, C, st), (self.k, self.kh, C // G, st),
+                          (self.v, self.vh, C // G, st)], P)
+            if e:
+                e[1].record()
+            U.attn_fwd(self.qh, self.kh, self.vh, w.H_q, w.H_kv, P, C, st, self.cu, w.causal,
+                       out=self.oh, lse=self._lse_stage(st))
+            if e:
+                e[2].record()
+            U.head2seq(self.oh, self.o, P, C, st)
+            if e:
+                e[3].record()
+                ev_f.append(e)
+        for st in range(self.stages):
+            e = marks()
+            if e:
+                e[0].record()
+            U.seq2head_n([(self.q, self.qh, C, st), (self.k, self.kh, C // G, st),
+                          (self.v, self.vh, C // G, st), (self.o, self.oh, C, st),
+                          (self.do, self.doh, C, st)], P)
+            if e:
+                e[1].record()
+            U.attn_bwd(self.qh, self.kh, self.vh, self.oh, self.doh, self._lse_stage(st), w.H_q, w.H_kv,
+                       P, C, st, self.cu, w.causal, workspace=self.ws, dq=self.dqh,
                        dk=self.dkh, dv=self.dvh)
-            if timed:
-                e3.record()
-            U.head2seq(self.dqh, self.dq, w.P, C, st)
-            U.head2seq(self.dkh, self.dk, w.P, C // G, st)
-            U.head2seq(self.dvh, self.dv, w.P, C // G, st)
-            if timed:
-                ev.append((e0, e1, e2, e3))
+            if e:
+                e[2].record()
+            U.head2seq_n([(self.dqh, self.dq, C, st), (self.dkh, self.dk, C // G, st),
+                          (self.dvh, self.dv, C // G, st)], P)
+            if e:
+                e[3].record()
+                ev_b.append(e)
         if timed:
-            self.events.append(ev)
+            self.events.append((ev_f, ev_b))
+
+    def durations(self):
+        """Mean per step of (forward attention, backward attention, all
+        re-layouts) in seconds, from the events of the timed steps."""
+        fw, bw, rl = [], [], []
+        for ev_f, ev_b in self.events:
+            f = sum(e[1].elapsed_time(e[2]) for e in ev_f) / 1e3
+            b = sum(e[1].elapsed_time(e[2]) for e in ev_b) / 1e3
+            r = sum(e[0].elapsed_time(e[1]) + e[2].elapsed_time(e[3]) for e in ev_f + ev_b) / 1e3
+            fw.append(f)
+            bw.append(b)
+            rl.append(r)
+        return statistics.mean(fw), statistics.mean(bw), statistics.mean(rl)
 
 
 def relayout_bytes_per_step(w):
+    """Bytes the step's re-layouts read plus write (STREAM-copy convention):
+    forward Q, K, V gathered and O scattered; backward Q, K, V, O, dO gathered
+    and the fp32 dQ, dK, dV scattered."""
     elt = 2 if w.dtype == "bf16" else 4
     n_q = w.B * w.S * w.H_q * w.D
     n_kv = w.B * w.S * w.H_kv * w.D
-    fwd = 2 * (n_q + 2 * n_kv) * elt + 2 * n_q * elt          # Q,K,V in; O out
-    bwd = 2 * n_q * elt + 2 * (n_q + 2 * n_kv) * 4            # dO in; dQ,dK,dV out (fp32)
-    # the step re-uses the forward's head-layout Q/K/V/O for the backward
+    fwd = 2 * (n_q + 2 * n_kv) * elt + 2 * n_q * elt
+    bwd = 2 * (3 * n_q + 2 * n_kv) * elt + 2 * (n_q + 2 * n_kv) * 4
     return fwd + bwd
 
 
@@ -514,13 +559,13 @@ def gpu_arm(args):
     if world > 1:
         dist.barrier()
     t_step = elapsed / args.steps
-    fwd_t = [sum(e0.elapsed_time(e1) for e0, e1, _, _ in ev) / 1e3 for ev in step.events]
-    bwd_t = [sum(e2.elapsed_time(e3) for _, _, e2, e3 in ev) / 1e3 for ev in step.events]
+    t_fwd, t_bwd, t_relayout = step.durations()
     n_launch_attn = step.stages
     pairs = pairs_total(w, cu_np) * w.H_q * w.B
     fl_fwd, fl_bwd = 4.0 * w.D * pairs, 10.0 * w.D * pairs
-    t_fwd, t_bwd = statistics.mean(fwd_t), statistics.mean(bwd_t)
     hbm, bf16, bf16_sus, peak_src = load_peaks()
+    relay_bytes = relayout_bytes_per_step(w)
+    relay_step_gbs = relay_bytes / t_relayout / 1e9
     relay_gbs = None
     e2e = None
     ring = None
@@ -542,16 +587,21 @@ def gpu_arm(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": t_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic N(0,1), seeded",
-        "config": {"workload": w.name, "S": w.S, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
-                   "D": w.D, "P": w.P, "head_chunk": w.head_chunk, "causal": w.causal,
-                   "packed": w.packed, "l2": "inputs larger than L2 (no flush needed)",
-                   "parallelism": f"{w.P} virtual ranks on one GPU" + (f", {world} replicas" if world > 1 else "")},
+        "config": workload_config(w, world),
         "tflops_fwd_bwd": (fl_fwd + fl_bwd) / (t_fwd + t_bwd) / 1e12,
         "attn_fwd_ms": t_fwd * 1e3, "attn_bwd_ms": t_bwd * 1e3,
         "attn_fwd_tflops": fl_fwd / t_fwd / 1e12, "attn_bwd_tflops": fl_bwd / t_bwd / 1e12,
         "frac_fwd_bwd_of_bf16_peak": (fl_fwd + fl_bwd) / (t_fwd + t_bwd) / 1e12 / bf16,
-        "relayout_gbs": relay_gbs, "relayout_frac_hbm": None if relay_gbs is None else relay_gbs / hbm,
-        "relayout_bytes_per_step": relayout_bytes_per_step(w),
+        "frac_fwd_bwd_of_nominal_bf16": (fl_fwd + fl_bwd) / (t_fwd + t_bwd) / 1e12 / NOMINAL_BF16_TFLOPS,
+        "peaks": {"bf16_tflops": bf16, "hbm_gbs": hbm, "source": peak_src,
+                  "nominal_bf16_tflops": NOMINAL_BF16_TFLOPS, "nominal_hbm_gbs": NOMINAL_HBM_GBS,
+                  "targets_judged_against": "the measured peaks (frac_* keys without 'nominal')"},
+        "relayout_gbs": relay_step_gbs, "relayout_frac_hbm": relay_step_gbs / hbm,
+        "relayout_ms_per_step": t_relayout * 1e3,
+        "relayout_bytes_per_step": relay_bytes,
+        "relayout_frac_nominal_hbm": relay_step_gbs / NOMINAL_HBM_GBS,
+        "relayout_isolated_q_gather_gbs": relay_gbs,
+        "relayout_isolated_q_gather_frac_hbm": None if relay_gbs is None else relay_gbs / hbm,
         "roofline": {"kernel": "attn_bwd", "bound": "tensor", "achieved": achieved,
                      "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
                      "traffic": measured_traffic(w.name),
@@ -595,12 +645,19 @@ def reference_arm(args):
            "warmup": args.warmup, "ms_per_step": statistics.median(secs) * 1e3,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic N(0,1), seeded", "impl": "reference",
-           "config": {"workload": w.name, "S": w.S, "H_q": w.H_q, "H_kv": w.H_kv, "D": w.D,
-                      "P": w.P, "head_chunk": w.head_chunk},
+           "config": workload_config(w, world),
            "cpu_baseline": {"value": v, "unit": UNIT, "cores": r["cores"], "kind": "oracle",
                             "sample": r["sample"]},
            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(res), flush=True)
+
+
+def workload_config(w, world):
+    """The `config` object of both arms' JSON lines (same keys, same values)."""
+    return {"workload": w.name, "S": w.S, "B": w.B, "H_q": w.H_q, "H_kv": w.H_kv,
+            "D": w.D, "P": w.P, "head_chunk": w.head_chunk, "causal": w.causal,
+            "packed": w.packed, "l2": "inputs larger than L2 (no flush needed)",
+            "parallelism": f"{w.P} virtual ranks on one GPU" + (f", {world} replicas" if world > 1 else "")}
 
 
 def workload_from_args(args):

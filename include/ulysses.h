@@ -139,6 +139,45 @@ int ulysses_lse_merge(float* o_acc, float* lse_acc, const void* o_part, const fl
 int ulysses_cast_f32(void* dst, const float* src, int64_t n, int dtype, void* stream);
 int ulysses_add_f32(float* dst, const float* src, int64_t n, void* stream);
 
+/* Ring variant of the whole layer, run natively (B == 1).  P virtual ranks;
+ * rank r keeps query chunk r (tokens [r L, (r+1) L), L = S / P) and meets KV
+ * chunk c = (r - t) mod P at ring step t.  Under a causal mask the chunks
+ * wholly in the future (c > r) are skipped, the diagonal step (c = r) is
+ * causal and the others are full; the steps' (O, LSE) are merged with
+ * ulysses_lse_merge's rule.  The backward runs every step with the merged LSE
+ * and O; the steps' partial dQ, dK, dV are summed in sequence layout.
+ *   q_seq/o_seq/do_seq [S][H_q][D], k_seq/v_seq [S][H_kv][D] in dtype;
+ *   lse  [P][H_q][L] fp32, chunk-major (written by fwd, read by bwd);
+ *   dq_seq [S][H_q][D], dk_seq/dv_seq [S][H_kv][D] fp32 (written by bwd);
+ *   workspace >= ulysses_ring_workspace() bytes, 256-byte aligned (the same
+ *   size serves both directions).
+ * S % P must be 0; H_q % H_kv == 0; D in {64, 128}. */
+size_t ulysses_ring_workspace(int64_t S, int H_q, int H_kv, int D, int P, int dtype);
+int ulysses_ring_fwd(const void* q_seq, const void* k_seq, const void* v_seq, void* o_seq, float* lse,
+                     int64_t S, int H_q, int H_kv, int D, int P, int causal, float scale, int dtype,
+                     void* workspace, size_t ws_bytes, void* stream);
+int ulysses_ring_bwd(const void* q_seq, const void* k_seq, const void* v_seq, const void* o_seq,
+                     const void* do_seq, const float* lse, float* dq_seq, float* dk_seq, float* dv_seq,
+                     int64_t S, int H_q, int H_kv, int D, int P, int causal, float scale, int dtype,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Padding to a multiple of the sequence-parallel degree (the pages' TRL
+ * section sets pad_to_multiple_of to the SP size).
+ * ulysses_pad_seq: x [B][S][H][D] -> x_pad [B][S_pad][H][D], the tokens
+ *   t >= S set to zero.  S_pad >= S; H*D*elt a multiple of 16 bytes; x and
+ *   x_pad must not overlap.
+ * ulysses_pad_cu_seqlens: cu_pad = the real documents' offsets (cu_seqlens,
+ *   num_docs + 1 entries, or [0, S] when cu_seqlens is NULL), followed by S_pad
+ *   when S_pad > S: the pad tokens form a document of their own, so no real
+ *   token attends to them or is attended by them.  cu_pad holds num_docs + 2
+ *   int32 (num_docs = 1 without a table); the padded table has one document
+ *   more than the real one when S_pad > S.  All pointers device pointers. */
+int ulysses_pad_seq(const void* x, void* x_pad, int64_t S, int64_t S_pad, int B, int H, int D, int dtype,
+                    void* stream);
+int ulysses_pad_cu_seqlens(const int32_t* cu_seqlens, int num_docs, int32_t* cu_pad, int64_t S, int64_t S_pad,
+                           void* stream);
+
 /* Self-test of the failure path shared by every kernel: launches one CTA that
  * waits on an mbarrier nothing arrives on, bounded by limit_ns (0 < limit_ns
  * <= 2e9).  The wait gives up, the kernel records ULYSSES_ERR_TIMEOUT in the
@@ -166,6 +205,32 @@ int ulysses_seq2head(const void* x_seq, void* x_head, int64_t S, int B, int H, i
  * heads of x_seq are written. */
 int ulysses_head2seq(const void* x_head, void* x_seq, int64_t S, int B, int H, int D, int P,
                      int head_chunk, int stage, int dtype, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Batched re-layout: several tensors of one stage in one launch (for example
+ * Q, K and V before a stage's forward, or dQ, dK and dV after its backward),
+ * so that the small K/V tensors share the launch and the tail of the large
+ * one.  Each item is one ulysses_seq2head / ulysses_head2seq call:
+ *   src, dst     as x_seq / x_head (seq2head) or x_head / x_seq (head2seq)
+ *   H, head_chunk, stage   as in the single calls
+ *   add          head2seq with ULYSSES_FP32 only: add into dst (as
+ *                ulysses_head2seq_add); must be 0 for seq2head
+ * All items share S, B, D, P and dtype; at most 6 items.  No item's
+ * destination may overlap any item's source (ULYSSES_ERR_INVALID).  The item
+ * array is read on the host during the call. */
+typedef struct {
+  const void* src;
+  void* dst;
+  int H;
+  int head_chunk;
+  int stage;
+  int add;
+} ulysses_relayout_item;
+
+int ulysses_seq2head_n(const ulysses_relayout_item* items, int n_items, int64_t S, int B, int D, int P,
+                       int dtype, void* stream);
+int ulysses_head2seq_n(const ulysses_relayout_item* items, int n_items, int64_t S, int B, int D, int P,
+                       int dtype, void* stream);
 
 /* As ulysses_head2seq, but adds the head rows into x_seq instead of writing
  * them (dtype must be ULYSSES_FP32).  Used for the gradients of a replicated
@@ -228,8 +293,10 @@ int ulysses_attn_bwd(const void* q_h, const void* k_h, const void* v_h, const vo
  *   Limit: B * (heads in the stage) * S <= 4,194,304 rows; larger shapes are
  *   rejected with ULYSSES_ERR_UNSUPPORTED (use ulysses_attn_bwd).
  *   The library itself allocates nothing here (no cudaMalloc/cudaFree).
- *   The first call on a device looks up the array's device address with that
- *   device current; make that first call before any stream capture.
+ *   Every call looks up the array's device address for the calling thread's
+ *   current device (a host-side lookup; the first one on a device may load
+ *   the library's device code, so make the first call on each device before
+ *   any stream capture).
  *   All calls share the one array: calls that overlap on the GPU (different
  *   streams, or host threads without ordering) race on it and must be
  *   serialised by the caller.  The array keeps the last call's D_i values;

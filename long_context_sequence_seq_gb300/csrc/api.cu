@@ -11,6 +11,7 @@
 #include <mutex>
 #include <cstdio>
 #include <cstring>
+#include <vector>
 
 #include <nvtx3/nvToolsExt.h>
 
@@ -53,6 +54,21 @@ int check_launch(const char* what) {
   if (e != cudaSuccess)
     return set_error(ULYSSES_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
   return ULYSSES_OK;
+}
+
+int opt_in_smem(PerDeviceOnce<>& once, const void* func, int bytes, const char* what) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(ULYSSES_ERR_CUDA, "%s: cudaGetDevice: %s", what, cudaGetErrorString(e));
+  const int rc = once.run(dev, [&]() -> int {
+    cudaError_t r = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (r != cudaSuccess)
+      return set_error(ULYSSES_ERR_CUDA, "%s: shared-memory opt-in of %d bytes on device %d: %s", what, bytes, dev,
+                       cudaGetErrorString(r));
+    return ULYSSES_OK;
+  }, -1);
+  if (rc == -1) return set_error(ULYSSES_ERR_UNSUPPORTED, "%s: device %d beyond the library's 64-device table", what, dev);
+  return rc;
 }
 
 // Error-word readers, one per translation unit that raises device errors.
@@ -119,8 +135,9 @@ int stage_span(int H, int P, int C, int stage, int* n, int* h0) {
   return ULYSSES_OK;
 }
 
-int relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, int D, int P,
-             int C, int stage, int dtype, void* stream, bool add = false) {
+// Validates one re-layout tensor and fills its job (heads moved, first head).
+int relayout_job(bool to_head, const void* src, void* dst, int64_t S, int B, int H, int D, int P, int C,
+                 int stage, int dtype, bool add, RelayoutJob* job) {
   const int elt = elt_size(dtype);
   if (!elt) return set_error(ULYSSES_ERR_INVALID, "unknown dtype %d", dtype);
   if (add && (to_head || dtype != ULYSSES_FP32))
@@ -132,14 +149,59 @@ int relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, 
   int n = 0, h0 = 0;
   int rc = stage_span(H, P, C, stage, &n, &h0);
   if (rc) return rc;
+  *job = RelayoutJob{src, dst, H, n, h0, add ? 1 : 0, 0};
   if (S == 0) return ULYSSES_OK;
   if (!src || !dst) return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
   if (!aligned16(src) || !aligned16(dst)) return set_error(ULYSSES_ERR_INVALID, "buffers must be 16-byte aligned");
-  const size_t seq_bytes = (size_t)B * S * H * D * elt, head_bytes = (size_t)B * n * S * D * elt;
-  const char* a = (const char*)src; const char* b = (const char*)dst;
-  size_t la = to_head ? seq_bytes : head_bytes, lb = to_head ? head_bytes : seq_bytes;
-  if (a < b + lb && b < a + la) return set_error(ULYSSES_ERR_INVALID, "re-layout cannot run in place");
-  return launch_relayout(to_head, src, dst, S, B, H, D, n, h0, elt, (cudaStream_t)stream, add);
+  return ULYSSES_OK;
+}
+
+// Byte ranges of a job's source and destination.
+void job_ranges(bool to_head, const RelayoutJob& j, int64_t S, int B, int D, int elt, const char** a, size_t* la,
+                const char** b, size_t* lb) {
+  const size_t seq_bytes = (size_t)B * S * j.H * D * elt, head_bytes = (size_t)B * j.n * S * D * elt;
+  *a = (const char*)j.src; *la = to_head ? seq_bytes : head_bytes;
+  *b = (const char*)j.dst; *lb = to_head ? head_bytes : seq_bytes;
+}
+
+bool overlap(const char* a, size_t la, const char* b, size_t lb) { return a < b + lb && b < a + la; }
+
+// A batch of re-layouts of one launch: every item's destination must be
+// disjoint from every item's source (the launch has no order among them).
+int relayout_n(bool to_head, const ulysses_relayout_item* items, int n_items, int64_t S, int B, int D, int P,
+               int dtype, void* stream) {
+  if (n_items < 0 || n_items > kMaxRelayoutJobs)
+    return set_error(ULYSSES_ERR_INVALID, "n_items=%d must be in [0, %d]", n_items, kMaxRelayoutJobs);
+  if (n_items > 0 && !items) return set_error(ULYSSES_ERR_INVALID, "NULL item list");
+  RelayoutBatch bt{};
+  for (int i = 0; i < n_items; ++i) {
+    const ulysses_relayout_item& it = items[i];
+    int rc = relayout_job(to_head, it.src, it.dst, S, B, it.H, D, P, it.head_chunk, it.stage, dtype,
+                          it.add != 0, &bt.job[i]);
+    if (rc) return rc;
+  }
+  if (S == 0 || n_items == 0) return ULYSSES_OK;
+  const int elt = elt_size(dtype);
+  for (int i = 0; i < n_items; ++i)
+    for (int k = 0; k < n_items; ++k) {
+      const char *ai, *bi, *ak, *bk;
+      size_t lai, lbi, lak, lbk;
+      job_ranges(to_head, bt.job[i], S, B, D, elt, &ai, &lai, &bi, &lbi);
+      job_ranges(to_head, bt.job[k], S, B, D, elt, &ak, &lak, &bk, &lbk);
+      if (overlap(bi, lbi, ak, lak))
+        return set_error(ULYSSES_ERR_INVALID, "re-layout cannot run in place (destination %d overlaps source %d)", i, k);
+    }
+  bt.njobs = n_items;
+  bt.S = S;
+  bt.B = B;
+  bt.V = D * elt / 16;
+  return launch_relayout_batch(to_head, bt, (cudaStream_t)stream);
+}
+
+int relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, int D, int P,
+             int C, int stage, int dtype, void* stream, bool add = false) {
+  ulysses_relayout_item it{src, dst, H, C, stage, add ? 1 : 0};
+  return relayout_n(to_head, &it, 1, S, B, D, P, dtype, stream);
 }
 
 // Shape validation shared by attention calls; fills a (without pointers).
@@ -229,28 +291,18 @@ LayerWs layer_ws(char* base, int64_t S, int B, int Cq, int Ckv, int D, int elt) 
 // in this file-scope device array instead of a caller-provided workspace.
 // Every device that loads the library holds it (16 MiB) until the process
 // exits.  In host code the symbol is only a stand-in, so its device address is
-// looked up once per device (with that device current) and passed to kernels.
+// looked up with the calling device current, on every call: the lookup is a
+// host-side table read once the library's device code is loaded, and it stays
+// right if the device's context is reset between calls.
 constexpr size_t kNoAllocDeltaFloats = size_t(1) << 22;   // 4,194,304 rows
 static __device__ __align__(256) float g_noalloc_delta[kNoAllocDeltaFloats];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[kMaxDevices] = {};
-
 int noalloc_scratch(float** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return set_error(ULYSSES_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kMaxDevices) return set_error(ULYSSES_ERR_UNSUPPORTED, "device %d beyond %d", dev, kMaxDevices);
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_delta);
-    if (e != cudaSuccess || p == nullptr)
-      return set_error(ULYSSES_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_noalloc_ptr[dev];
+  void* p = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_delta);
+  if (e != cudaSuccess || p == nullptr)
+    return set_error(ULYSSES_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+  *out = static_cast<float*>(p);
   return ULYSSES_OK;
 }
 
@@ -436,6 +488,18 @@ int ulysses_head2seq(const void* x_head, void* x_seq, int64_t S, int B, int H, i
   return relayout(false, x_head, x_seq, S, B, H, D, P, head_chunk, stage, dtype, stream);
 }
 
+int ulysses_seq2head_n(const ulysses_relayout_item* items, int n_items, int64_t S, int B, int D, int P,
+                       int dtype, void* stream) {
+  for (int i = 0; i < n_items && items; ++i)
+    if (items[i].add) return set_error(ULYSSES_ERR_UNSUPPORTED, "accumulating re-layout is head->seq, fp32 only");
+  return relayout_n(true, items, n_items, S, B, D, P, dtype, stream);
+}
+
+int ulysses_head2seq_n(const ulysses_relayout_item* items, int n_items, int64_t S, int B, int D, int P,
+                       int dtype, void* stream) {
+  return relayout_n(false, items, n_items, S, B, D, P, dtype, stream);
+}
+
 int ulysses_head2seq_add(const void* x_head, void* x_seq, int64_t S, int B, int H, int D, int P,
                          int head_chunk, int stage, int dtype, void* stream) {
   return relayout(false, x_head, x_seq, S, B, H, D, P, head_chunk, stage, dtype, stream, true);
@@ -543,9 +607,10 @@ int ulysses_layer_fwd(const void* q_seq, const void* k_seq, const void* v_seq, v
     int n = 0, h0 = 0;
     stage_span(H_q, P, C, s, &n, &h0);
     const int ks = kv_stage(H_kv, P, s, stages);
-    if ((rc = relayout(true, q_seq, w.qh, S, B, H_q, D, P, C, s, dtype, stream))) return rc;
-    if ((rc = relayout(true, k_seq, w.kh, S, B, H_kv, D, P, Ckv, ks, dtype, stream))) return rc;
-    if ((rc = relayout(true, v_seq, w.vh, S, B, H_kv, D, P, Ckv, ks, dtype, stream))) return rc;
+    const ulysses_relayout_item gather[3] = {{q_seq, w.qh, H_q, C, s, 0},
+                                             {k_seq, w.kh, H_kv, Ckv, ks, 0},
+                                             {v_seq, w.vh, H_kv, Ckv, ks, 0}};
+    if ((rc = relayout_n(true, gather, 3, S, B, D, P, dtype, stream))) return rc;
     AttnArgs sa = a;
     sa.q = w.qh; sa.k = w.kh; sa.v = w.vh; sa.o_out = w.oh;
     sa.lse = lse + (size_t)h0 * S;
@@ -581,11 +646,12 @@ int ulysses_layer_bwd(const void* q_seq, const void* k_seq, const void* v_seq, c
     int n = 0, h0 = 0;
     stage_span(H_q, P, C, s, &n, &h0);
     const int ks = kv_stage(H_kv, P, s, stages);
-    if ((rc = relayout(true, q_seq, w.qh, S, B, H_q, D, P, C, s, dtype, stream))) return rc;
-    if ((rc = relayout(true, k_seq, w.kh, S, B, H_kv, D, P, Ckv, ks, dtype, stream))) return rc;
-    if ((rc = relayout(true, v_seq, w.vh, S, B, H_kv, D, P, Ckv, ks, dtype, stream))) return rc;
-    if ((rc = relayout(true, o_seq, w.oh, S, B, H_q, D, P, C, s, dtype, stream))) return rc;
-    if ((rc = relayout(true, do_seq, w.doh, S, B, H_q, D, P, C, s, dtype, stream))) return rc;
+    const ulysses_relayout_item gather[5] = {{q_seq, w.qh, H_q, C, s, 0},
+                                             {k_seq, w.kh, H_kv, Ckv, ks, 0},
+                                             {v_seq, w.vh, H_kv, Ckv, ks, 0},
+                                             {o_seq, w.oh, H_q, C, s, 0},
+                                             {do_seq, w.doh, H_q, C, s, 0}};
+    if ((rc = relayout_n(true, gather, 5, S, B, D, P, dtype, stream))) return rc;
     AttnArgs sa = a;
     sa.q = w.qh; sa.k = w.kh; sa.v = w.vh; sa.o = w.oh; sa.dO = w.doh;
     sa.lse_in = lse + (size_t)h0 * S;
@@ -593,12 +659,174 @@ int ulysses_layer_bwd(const void* q_seq, const void* k_seq, const void* v_seq, c
     sa.dq = w.dqh; sa.dk = w.dkh; sa.dv = w.dvh; sa.delta = w.delta;
     rc = use_tc_bwd(sa) ? launch_tc_bwd(sa, st) : launch_simt_bwd(sa, st);
     if (rc) return rc;
-    if ((rc = relayout(false, w.dqh, dq_seq, S, B, H_q, D, P, C, s, ULYSSES_FP32, stream))) return rc;
     // with kv-head replication every stage holds a partial dK/dV of its kv
     // head: the head's first stage writes it, the later ones add to it
-    const bool add = H_kv < P && !kv_first_stage(H_kv, P, s, stages);
-    if ((rc = relayout(false, w.dkh, dk_seq, S, B, H_kv, D, P, Ckv, ks, ULYSSES_FP32, stream, add))) return rc;
-    if ((rc = relayout(false, w.dvh, dv_seq, S, B, H_kv, D, P, Ckv, ks, ULYSSES_FP32, stream, add))) return rc;
+    const int add = (H_kv < P && !kv_first_stage(H_kv, P, s, stages)) ? 1 : 0;
+    const ulysses_relayout_item scatter[3] = {{w.dqh, dq_seq, H_q, C, s, 0},
+                                              {w.dkh, dk_seq, H_kv, Ckv, ks, add},
+                                              {w.dvh, dv_seq, H_kv, Ckv, ks, add}};
+    if ((rc = relayout_n(false, scatter, 3, S, B, D, P, ULYSSES_FP32, stream))) return rc;
+  }
+  return ULYSSES_OK;
+}
+
+}  // extern "C"
+
+namespace {
+// ---------------------------------------------------------------------------
+// Ring-attention variant driven natively: rank r keeps query chunk r and meets
+// KV chunk (r - t) mod P at ring step t.
+struct RingWs {
+  char *qh, *kh, *vh, *oh, *doh;
+  float *o_acc, *lse_part, *dqh, *dkh, *dvh, *delta;
+  size_t total;
+};
+
+RingWs ring_ws(char* base, int64_t L, int Hq, int Hkv, int D, int elt) {
+  RingWs w{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) { char* p = base ? base + off : nullptr; off += align256(bytes); return p; };
+  const size_t q_n = (size_t)Hq * L * D, kv_n = (size_t)Hkv * L * D;
+  w.qh = take(q_n * elt); w.kh = take(kv_n * elt); w.vh = take(kv_n * elt);
+  w.oh = take(q_n * elt); w.doh = take(q_n * elt);
+  w.o_acc = (float*)take(q_n * 4); w.lse_part = (float*)take((size_t)Hq * L * 4);
+  w.dqh = (float*)take(q_n * 4); w.dkh = (float*)take(kv_n * 4); w.dvh = (float*)take(kv_n * 4);
+  w.delta = (float*)take((size_t)Hq * L * 4);
+  w.total = off;
+  return w;
+}
+
+int ring_shape(AttnArgs& a, int64_t S, int H_q, int H_kv, int D, int P, int causal, float scale, int dtype) {
+  if (P <= 0 || S < 0 || S % P) return set_error(ULYSSES_ERR_INVALID, "S=%lld not divisible by P=%d", (long long)S, P);
+  return attn_shape(a, S / P, 1, H_q, H_kv, D, 1, 0, -1, nullptr, 0, causal, scale, dtype);
+}
+
+}  // namespace
+
+extern "C" {
+
+// ---------------------------------------------------------------------------
+// Padding to a multiple of P (pad_to_multiple_of in the TRL section).
+int ulysses_pad_seq(const void* x, void* x_pad, int64_t S, int64_t S_pad, int B, int H, int D, int dtype,
+                    void* stream) {
+  const int elt = elt_size(dtype);
+  if (!elt) return set_error(ULYSSES_ERR_INVALID, "unknown dtype %d", dtype);
+  if (S < 0 || S_pad < S || B <= 0 || H <= 0 || D <= 0)
+    return set_error(ULYSSES_ERR_INVALID, "bad sizes S=%lld S_pad=%lld B=%d H=%d D=%d", (long long)S,
+                     (long long)S_pad, B, H, D);
+  const int64_t row = (int64_t)H * D * elt;
+  if (row % 16) return set_error(ULYSSES_ERR_UNSUPPORTED, "H*D*elt=%lld must be a multiple of 16 bytes", (long long)row);
+  if (S_pad == 0) return ULYSSES_OK;
+  if (!x_pad || (S > 0 && !x)) return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  if (!aligned16(x_pad) || (S > 0 && !aligned16(x))) return set_error(ULYSSES_ERR_INVALID, "buffers must be 16-byte aligned");
+  if (S > 0 && overlap((const char*)x, (size_t)B * S * row, (const char*)x_pad, (size_t)B * S_pad * row))
+    return set_error(ULYSSES_ERR_INVALID, "padding cannot run in place");
+  return launch_pad_seq(x, x_pad, S, S_pad, B, row, (cudaStream_t)stream);
+}
+
+int ulysses_pad_cu_seqlens(const int32_t* cu_seqlens, int num_docs, int32_t* cu_pad, int64_t S, int64_t S_pad,
+                           void* stream) {
+  if (S < 0 || S_pad < S || S_pad > ((int64_t)1 << 31) - 1)
+    return set_error(ULYSSES_ERR_INVALID, "bad sizes S=%lld S_pad=%lld", (long long)S, (long long)S_pad);
+  if (cu_seqlens && num_docs <= 0) return set_error(ULYSSES_ERR_INVALID, "num_docs must be >= 1 with cu_seqlens");
+  if (!cu_pad) return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  return launch_pad_cu(cu_seqlens, cu_seqlens ? num_docs : 1, cu_pad, S, S_pad, (cudaStream_t)stream);
+}
+
+size_t ulysses_ring_workspace(int64_t S, int H_q, int H_kv, int D, int P, int dtype) {
+  AttnArgs a;
+  if (ring_shape(a, S, H_q, H_kv, D, P, 1, 0.f, dtype)) return 0;
+  return ring_ws(nullptr, S / P, H_q, H_kv, D, elt_size(dtype)).total;
+}
+
+int ulysses_ring_fwd(const void* q_seq, const void* k_seq, const void* v_seq, void* o_seq, float* lse,
+                     int64_t S, int H_q, int H_kv, int D, int P, int causal, float scale, int dtype,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  AttnArgs a;
+  int rc = ring_shape(a, S, H_q, H_kv, D, P, causal, scale, dtype);
+  if (rc) return rc;
+  if (S == 0) return ULYSSES_OK;
+  if (!q_seq || !k_seq || !v_seq || !o_seq || !lse || !workspace) return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  const int elt = elt_size(dtype);
+  const int64_t L = S / P;
+  RingWs w = ring_ws((char*)workspace, L, H_q, H_kv, D, elt);
+  if (ws_bytes < w.total) return set_error(ULYSSES_ERR_INVALID, "workspace too small: %zu < %zu", ws_bytes, w.total);
+  if (((uintptr_t)workspace & 255u) != 0) return set_error(ULYSSES_ERR_INVALID, "workspace must be 256-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t q_chunk = (size_t)L * H_q * D * elt, kv_chunk = (size_t)L * H_kv * D * elt;
+  for (int r = 0; r < P; ++r) {
+    StageRange range("ring fwd rank", r);
+    if ((rc = relayout(true, (const char*)q_seq + r * q_chunk, w.qh, L, 1, H_q, D, 1, 0, -1, dtype, stream)))
+      return rc;
+    float* lse_r = lse + (size_t)r * H_q * L;
+    int first = 1;
+    for (int t = 0; t < P; ++t) {
+      const int c = (r - t + P) % P;
+      if (causal && c > r) continue;                 // a chunk wholly in the future
+      const ulysses_relayout_item kv[2] = {{(const char*)k_seq + c * kv_chunk, w.kh, H_kv, 0, -1, 0},
+                                           {(const char*)v_seq + c * kv_chunk, w.vh, H_kv, 0, -1, 0}};
+      if ((rc = relayout_n(true, kv, 2, L, 1, D, 1, dtype, stream))) return rc;
+      AttnArgs sa = a;
+      sa.causal = (causal && c == r) ? 1 : 0;       // the diagonal step is causal, the others full
+      sa.q = w.qh; sa.k = w.kh; sa.v = w.vh; sa.o_out = w.oh; sa.lse = w.lse_part;
+      if ((rc = run_fwd(sa, st))) return rc;
+      if ((rc = launch_lse_merge(w.o_acc, lse_r, w.oh, w.lse_part, (int64_t)H_q * L, D, dtype, first, st)))
+        return rc;
+      first = 0;
+    }
+    if ((rc = launch_cast_f32(w.oh, w.o_acc, (int64_t)H_q * L * D, dtype, st))) return rc;
+    if ((rc = relayout(false, w.oh, (char*)o_seq + r * q_chunk, L, 1, H_q, D, 1, 0, -1, dtype, stream))) return rc;
+  }
+  return ULYSSES_OK;
+}
+
+int ulysses_ring_bwd(const void* q_seq, const void* k_seq, const void* v_seq, const void* o_seq,
+                     const void* do_seq, const float* lse, float* dq_seq, float* dk_seq, float* dv_seq,
+                     int64_t S, int H_q, int H_kv, int D, int P, int causal, float scale, int dtype,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  AttnArgs a;
+  int rc = ring_shape(a, S, H_q, H_kv, D, P, causal, scale, dtype);
+  if (rc) return rc;
+  if (S == 0) return ULYSSES_OK;
+  if (!q_seq || !k_seq || !v_seq || !o_seq || !do_seq || !lse || !dq_seq || !dk_seq || !dv_seq || !workspace)
+    return set_error(ULYSSES_ERR_INVALID, "NULL buffer");
+  if (P > 4096) return set_error(ULYSSES_ERR_UNSUPPORTED, "P=%d above 4096 ring ranks", P);
+  const int elt = elt_size(dtype);
+  const int64_t L = S / P;
+  RingWs w = ring_ws((char*)workspace, L, H_q, H_kv, D, elt);
+  if (ws_bytes < w.total) return set_error(ULYSSES_ERR_INVALID, "workspace too small: %zu < %zu", ws_bytes, w.total);
+  if (((uintptr_t)workspace & 255u) != 0) return set_error(ULYSSES_ERR_INVALID, "workspace must be 256-byte aligned");
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t q_chunk = (size_t)L * H_q * D * elt, kv_chunk = (size_t)L * H_kv * D * elt;
+  const size_t qf_chunk = (size_t)L * H_q * D, kvf_chunk = (size_t)L * H_kv * D;   // fp32 elements
+  std::vector<char> kv_seen(P, 0);
+  for (int r = 0; r < P; ++r) {
+    StageRange range("ring bwd rank", r);
+    const ulysses_relayout_item qod[3] = {{(const char*)q_seq + r * q_chunk, w.qh, H_q, 0, -1, 0},
+                                          {(const char*)o_seq + r * q_chunk, w.oh, H_q, 0, -1, 0},
+                                          {(const char*)do_seq + r * q_chunk, w.doh, H_q, 0, -1, 0}};
+    if ((rc = relayout_n(true, qod, 3, L, 1, D, 1, dtype, stream))) return rc;
+    bool q_seen = false;
+    for (int t = 0; t < P; ++t) {
+      const int c = (r - t + P) % P;
+      if (causal && c > r) continue;
+      const ulysses_relayout_item kv[2] = {{(const char*)k_seq + c * kv_chunk, w.kh, H_kv, 0, -1, 0},
+                                           {(const char*)v_seq + c * kv_chunk, w.vh, H_kv, 0, -1, 0}};
+      if ((rc = relayout_n(true, kv, 2, L, 1, D, 1, dtype, stream))) return rc;
+      AttnArgs sa = a;
+      sa.causal = (causal && c == r) ? 1 : 0;
+      sa.q = w.qh; sa.k = w.kh; sa.v = w.vh; sa.o = w.oh; sa.dO = w.doh;
+      sa.lse_in = lse + (size_t)r * H_q * L;        // the merged LSE of query chunk r
+      sa.dq = w.dqh; sa.dk = w.dkh; sa.dv = w.dvh; sa.delta = w.delta;
+      if ((rc = run_bwd(sa, st))) return rc;
+      // the step's partial gradients: the first one of a chunk writes, the rest add
+      const ulysses_relayout_item g[3] = {{w.dqh, dq_seq + r * qf_chunk, H_q, 0, -1, q_seen ? 1 : 0},
+                                          {w.dkh, dk_seq + c * kvf_chunk, H_kv, 0, -1, kv_seen[c] ? 1 : 0},
+                                          {w.dvh, dv_seq + c * kvf_chunk, H_kv, 0, -1, kv_seen[c] ? 1 : 0}};
+      if ((rc = relayout_n(false, g, 3, L, 1, D, 1, ULYSSES_FP32, stream))) return rc;
+      q_seen = true;
+      kv_seen[c] = 1;
+    }
   }
   return ULYSSES_OK;
 }

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "device_once.h"
+
 namespace ulysses {
 
 // Arguments of one attention launch on head-layout buffers (batch folded into
@@ -27,6 +29,31 @@ struct AttnArgs {
   int seq; int hq_tot; int hkv_tot;
 };
 
+// Opts `func` in to `bytes` of dynamic shared memory on the current device,
+// once per device (the runtime records the attribute per device); reports
+// ULYSSES_ERR_CUDA with a message when the runtime refuses.  api.cu.
+int opt_in_smem(PerDeviceOnce<>& once, const void* func, int bytes, const char* what);
+
+// One tensor of a batched re-layout launch (relayout.cu): moves n heads
+// starting at h0 of a sequence-layout tensor with H heads to or from a
+// head-layout buffer; `add` (scatter, fp32 only) adds instead of writing.
+// x0 is filled in by the launcher.
+constexpr int kMaxRelayoutJobs = 6;
+struct RelayoutJob {
+  const void* src; void* dst;
+  int H, n, h0, add;
+  int x0;
+};
+// Tensors of one launch share S, B and the row size V (16-byte words per
+// D-vector).
+struct RelayoutBatch {
+  RelayoutJob job[kMaxRelayoutJobs];
+  int njobs;
+  int B;
+  int V;
+  int64_t S;
+};
+int launch_relayout_batch(bool to_head, RelayoutBatch& bt, cudaStream_t stream);
 int launch_relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, int D,
                     int n, int h0, int elt, cudaStream_t stream, bool add = false);
 int launch_simt_fwd(const AttnArgs& a, cudaStream_t st);
@@ -37,6 +64,9 @@ int launch_lse_merge(float* o_acc, float* lse_acc, const void* o_part, const flo
                      int D, int dtype, int first, cudaStream_t st);                       // ring.cu
 int launch_cast_f32(void* dst, const float* src, int64_t n, int dtype, cudaStream_t st);  // ring.cu
 int launch_add_f32(float* dst, const float* src, int64_t n, cudaStream_t st);             // ring.cu
+int launch_pad_seq(const void* x, void* x_pad, int64_t S, int64_t S_pad, int B, int64_t row_bytes,
+                   cudaStream_t st);                                                      // pad.cu
+int launch_pad_cu(const int32_t* cu, int nd, int32_t* out, int64_t S, int64_t S_pad, cudaStream_t st);  // pad.cu
 int launch_qkv_proj(const void* x, const void* w, void* qkv_head, int64_t S, int hidden, int n_heads, int D,
                     cudaStream_t st);                                                     // proj_gemm.cu
 int launch_out_proj(const void* o_head, const void* w, void* y, int64_t S, int H_q, int D, int hidden,

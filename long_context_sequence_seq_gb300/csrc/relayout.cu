@@ -7,16 +7,25 @@
 // The scatter also has an accumulating form (fp32), X_seq += X_head, which
 // sums the partial dK/dV of stages that share a replicated kv head.
 //
-// The unit moved is one D-vector (128-512 bytes), copied as 16-byte words, so
-// both the read and the write side are fully coalesced.  The kernel is a pure
-// HBM stream: 2 * bytes moved per call, no arithmetic.  Bit-exact by
-// construction (raw 16-byte words, any element type).
+// One launch moves a batch of up to kMaxJobs tensors of one stage (Q, K and V
+// of a forward stage; Q, K, V, O and dO of a backward stage; dQ, dK and dV),
+// so the small K/V tensors do not pay a launch and a tail of their own.  The
+// grid is two-dimensional: blockIdx.x = (tensor, batch entry, head), fastest,
+// so CTAs that run together read neighbouring heads of the same tokens;
+// blockIdx.y = a block of tokens.  A thread block is (words of a row) x (rows):
+// the unit moved is one D-vector (128-512 bytes) as 16-byte words, so both
+// sides are coalesced, and no division runs per word (one per CTA).  The
+// kernel is a pure HBM stream: 2 * bytes moved per call, no arithmetic.
+// Bit-exact by construction (raw 16-byte words, any element type).
 #include "common.cuh"
+#include "internal.h"
 
 namespace ulysses {
 
-// Each thread moves kUnroll 16-byte words per iteration of a grid-stride loop.
-constexpr int kUnroll = 4;
+namespace {
+
+constexpr int kRows = 4;          // rows per thread per token block (loads in flight)
+constexpr int kThreads = 256;
 
 __device__ __forceinline__ int4 ld_stream(const int4* p) {
   int4 v;
@@ -25,81 +34,88 @@ __device__ __forceinline__ int4 ld_stream(const int4* p) {
   return v;
 }
 
+__device__ __forceinline__ int4 add_f32x4(int4 a, int4 b) {
+  return make_int4(__float_as_int(__int_as_float(a.x) + __int_as_float(b.x)),
+                   __float_as_int(__int_as_float(a.y) + __int_as_float(b.y)),
+                   __float_as_int(__int_as_float(a.z) + __int_as_float(b.z)),
+                   __float_as_int(__int_as_float(a.w) + __int_as_float(b.w)));
+}
+
 // to_head = true:  seq -> head (gather)   to_head = false: head -> seq (scatter)
-// kAdd (scatter only): add the fp32 head rows into the sequence rows
-template <bool kToHead, bool kAdd = false>
-__global__ void __launch_bounds__(256) relayout_kernel(const int4* __restrict__ src,
-                                                       int4* __restrict__ dst, int64_t S,
-                                                       int n, int H, int h0, int vec_per_row,
-                                                       int64_t total_vecs) {
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  // index o enumerates the head layout [B][n][S][V] (V = 16-byte words per row)
-  for (; base < total_vecs; base += stride * kUnroll) {
-    int4 val[kUnroll];
-    int64_t seq_idx[kUnroll], head_idx[kUnroll];
+template <bool kToHead>
+__global__ void __launch_bounds__(kThreads) relayout_kernel(const __grid_constant__ RelayoutBatch bt) {
+  // the job (tensor) of this CTA: the last one whose first column is <= x
+  const int x = blockIdx.x;
+  int j = 0;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      int64_t o = base + (int64_t)u * stride;
-      head_idx[u] = o;
-      if (o < total_vecs) {
-        int64_t v = o % vec_per_row;
-        int64_t row = o / vec_per_row;        // ((b*n + hh)*S + t)
-        int64_t t = row % S;
-        int64_t bh = row / S;
-        int64_t hh = bh % n;
-        int64_t b = bh / n;
-        seq_idx[u] = (((b * S + t) * H) + h0 + hh) * vec_per_row + v;
+  for (int k = 1; k < kMaxRelayoutJobs; ++k)
+    if (k < bt.njobs && x >= bt.job[k].x0) j = k;
+  const RelayoutJob& jb = bt.job[j];
+  const int bh = x - jb.x0;                 // b * n + hh
+  const int b = bh / jb.n, hh = bh - b * jb.n;
+  const int V = bt.V;
+  const int64_t S = bt.S;
+  const int4* __restrict__ src = reinterpret_cast<const int4*>(jb.src);
+  int4* __restrict__ dst = reinterpret_cast<int4*>(jb.dst);
+  // word offsets of token 0 of this (b, head) on both sides, and the step
+  // between consecutive tokens
+  const int64_t head_base = (int64_t)bh * S * V;
+  const int64_t seq_base = ((int64_t)b * S * jb.H + jb.h0 + hh) * V;
+  const int64_t seq_step = (int64_t)jb.H * V;
+  const int rows_per_blk = blockDim.y * kRows;
+  for (int64_t tb = blockIdx.y; tb * rows_per_blk < S; tb += gridDim.y) {
+    const int64_t t0 = tb * rows_per_blk + threadIdx.y;
+    for (int v = threadIdx.x; v < V; v += blockDim.x) {
+      int4 val[kRows];
+#pragma unroll
+      for (int u = 0; u < kRows; ++u) {
+        const int64_t t = t0 + (int64_t)u * blockDim.y;
+        if (t < S) val[u] = ld_stream(src + (kToHead ? seq_base + t * seq_step : head_base + t * V) + v);
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (head_idx[u] < total_vecs)
-        val[u] = ld_stream(src + (kToHead ? seq_idx[u] : head_idx[u]));
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (head_idx[u] < total_vecs) {
-        if (kAdd) {
-          int4* p = dst + seq_idx[u];
-          const int4 o = *p;
-          val[u] = make_int4(__float_as_int(__int_as_float(o.x) + __int_as_float(val[u].x)),
-                             __float_as_int(__int_as_float(o.y) + __int_as_float(val[u].y)),
-                             __float_as_int(__int_as_float(o.z) + __int_as_float(val[u].z)),
-                             __float_as_int(__int_as_float(o.w) + __int_as_float(val[u].w)));
-          *p = val[u];
-        } else {
-          dst[kToHead ? head_idx[u] : seq_idx[u]] = val[u];
+      for (int u = 0; u < kRows; ++u) {
+        const int64_t t = t0 + (int64_t)u * blockDim.y;
+        if (t < S) {
+          int4* p = dst + (kToHead ? head_base + t * V : seq_base + t * seq_step) + v;
+          if (!kToHead && jb.add) *p = add_f32x4(*p, val[u]);
+          else *p = val[u];
         }
       }
     }
   }
 }
 
-int launch_relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, int D,
-                    int n, int h0, int elt, cudaStream_t stream, bool add) {
-  const int row_bytes = D * elt;
-  const int vec_per_row = row_bytes / 16;
-  const int64_t total = (int64_t)B * n * S * vec_per_row;
-  if (total == 0) return ULYSSES_OK;
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int threads = 256;
-  int64_t want = (total + (int64_t)threads * kUnroll - 1) / ((int64_t)threads * kUnroll);
-  int64_t cap = (int64_t)sms * 8;  // 8 CTAs of 256 threads per SM: full occupancy
-  int blocks = (int)(want < cap ? want : cap);
+}  // namespace
+
+int launch_relayout_batch(bool to_head, RelayoutBatch& bt, cudaStream_t stream) {
+  if (bt.njobs <= 0 || bt.S == 0) return ULYSSES_OK;
+  int cols = 0;
+  for (int k = 0; k < bt.njobs; ++k) {
+    bt.job[k].x0 = cols;
+    cols += bt.B * bt.job[k].n;
+  }
+  const int bx = bt.V < kThreads ? bt.V : kThreads;
+  const int by = kThreads / bx;
+  const int64_t n_tb = (bt.S + (int64_t)by * kRows - 1) / ((int64_t)by * kRows);
+  dim3 block((unsigned)bx, (unsigned)by);
+  dim3 grid((unsigned)cols, (unsigned)(n_tb < 65535 ? n_tb : 65535));
   if (to_head)
-    relayout_kernel<true><<<blocks, threads, 0, stream>>>(
-        (const int4*)src, (int4*)dst, S, n, H, h0, vec_per_row, total);
-  else if (add)
-    relayout_kernel<false, true><<<blocks, threads, 0, stream>>>(
-        (const int4*)src, (int4*)dst, S, n, H, h0, vec_per_row, total);
+    relayout_kernel<true><<<grid, block, 0, stream>>>(bt);
   else
-    relayout_kernel<false><<<blocks, threads, 0, stream>>>(
-        (const int4*)src, (int4*)dst, S, n, H, h0, vec_per_row, total);
+    relayout_kernel<false><<<grid, block, 0, stream>>>(bt);
   count_launch();
   return check_launch("relayout");
+}
+
+int launch_relayout(bool to_head, const void* src, void* dst, int64_t S, int B, int H, int D,
+                    int n, int h0, int elt, cudaStream_t stream, bool add) {
+  RelayoutBatch bt{};
+  bt.njobs = 1;
+  bt.S = S;
+  bt.B = B;
+  bt.V = D * elt / 16;
+  bt.job[0] = RelayoutJob{src, dst, H, n, h0, add ? 1 : 0, 0};
+  return launch_relayout_batch(to_head, bt, stream);
 }
 
 }  // namespace ulysses

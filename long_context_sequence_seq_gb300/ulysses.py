@@ -25,6 +25,12 @@ KERNEL_AUTO, KERNEL_SIMT = 0, 1
 _lib = None
 
 
+class RelayoutItem(ctypes.Structure):
+    """ulysses_relayout_item: one tensor of a batched re-layout launch."""
+    _fields_ = [("src", ctypes.c_void_p), ("dst", ctypes.c_void_p), ("H", ctypes.c_int),
+                ("head_chunk", ctypes.c_int), ("stage", ctypes.c_int), ("add", ctypes.c_int)]
+
+
 class UlyssesError(RuntimeError):
     def __init__(self, code, msg):
         super().__init__(f"ulysses error {code}: {msg}")
@@ -44,7 +50,16 @@ def lib():
     L.ulysses_seq2head.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
     L.ulysses_head2seq.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
     L.ulysses_head2seq_add.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
+    L.ulysses_seq2head_n.argtypes = [ctypes.POINTER(RelayoutItem), i32, i64, i32, i32, i32, i32, vp]
+    L.ulysses_head2seq_n.argtypes = [ctypes.POINTER(RelayoutItem), i32, i64, i32, i32, i32, i32, vp]
     L.ulysses_selftest_wait_timeout.argtypes = [i64, vp]
+    L.ulysses_ring_workspace.argtypes = [i64, i32, i32, i32, i32, i32]
+    L.ulysses_ring_workspace.restype = sz
+    L.ulysses_ring_fwd.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, f32, i32, vp, sz, vp]
+    L.ulysses_ring_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i32, i32, f32, i32,
+                                   vp, sz, vp]
+    L.ulysses_pad_seq.argtypes = [vp, vp, i64, i64, i32, i32, i32, i32, vp]
+    L.ulysses_pad_cu_seqlens.argtypes = [vp, i32, vp, i64, i64, vp]
     L.ulysses_lse_merge.argtypes = [vp, vp, vp, vp, i64, i32, i32, i32, vp]
     L.ulysses_cast_f32.argtypes = [vp, vp, i64, i32, vp]
     L.ulysses_add_f32.argtypes = [vp, vp, i64, vp]
@@ -153,27 +168,64 @@ def head2seq_add(x_head, x_seq, P, head_chunk=None, stage=None, stream=None):
     return x_seq
 
 
-def pad_to_multiple(tensors, P, cu_seqlens=None):
-    """Pad [B,S,H,D] tensors along S to a multiple of P (as pad_to_multiple_of
-    does for sequence parallelism).  Returns (padded tensors, cu_seqlens, S):
-    the padding positions form a document of their own, so no real position
-    attends to them or is attended by them (S stays the caller's length for
-    slicing the results back).  cu_seqlens (int32, device) describes the real
-    documents, or None for one document; it is needed with B == 1 only."""
+def _relayout_n(fn, pairs, P, stream, head_seq_index):
+    """pairs: (src, dst, head_chunk, stage[, add]) per tensor; the sequence-
+    layout tensor of each pair gives S, B, H, D (head_seq_index picks it)."""
+    if not pairs:
+        return
+    items = (RelayoutItem * len(pairs))()
+    seq0 = pairs[0][head_seq_index]
+    B, S, _, D = seq0.shape
+    dt = _dtype_code(seq0)
+    for i, pr in enumerate(pairs):
+        src, dst, C, stage = pr[:4]
+        add = pr[4] if len(pr) > 4 else 0
+        seq = pr[head_seq_index]
+        if _dtype_code(src) != dt or _dtype_code(dst) != dt:
+            raise TypeError("every tensor of a batched re-layout has the same dtype")
+        items[i] = RelayoutItem(_p(src).value, _p(dst).value, seq.shape[2], C or 0, _stage(stage), int(add))
+    _ck(fn(items, len(pairs), S, B, D, P, dt, _stream(stream)))
+
+
+def seq2head_n(pairs, P, stream=None):
+    """Batched all-to-all #1, one launch: pairs of (x_seq [B,S,H,D], x_head
+    [B,n,S,D] out, head_chunk, stage) sharing S, B, D and dtype."""
+    _relayout_n(lib().ulysses_seq2head_n, pairs, P, stream, 0)
+
+
+def head2seq_n(pairs, P, stream=None):
+    """Batched all-to-all #2, one launch: (x_head, x_seq, head_chunk, stage[,
+    add]) per tensor; add (fp32 only) accumulates into x_seq."""
+    _relayout_n(lib().ulysses_head2seq_n, pairs, P, stream, 1)
+
+
+def padded_length(S, P):
+    """S rounded up to a multiple of P."""
+    return (S + P - 1) // P * P
+
+
+def pad_to_multiple(tensors, P, cu_seqlens=None, stream=None):
+    """Pad [B,S,H,D] device tensors along S to a multiple of P (as
+    pad_to_multiple_of does for sequence parallelism) with the library's pad
+    kernels.  Returns (padded tensors, cu_seqlens, S): the padding positions
+    form a document of their own, so no real position attends to them or is
+    attended by them (S stays the caller's length for slicing the results
+    back).  cu_seqlens (int32, device) describes the real documents, or None
+    for one document; it is needed with B == 1 only."""
     S = tensors[0].shape[1]
-    S_pad = (S + P - 1) // P * P
+    S_pad = padded_length(S, P)
     if S_pad == S:
         return list(tensors), cu_seqlens, S
     out = []
     for t in tensors:
-        p = torch.zeros((t.shape[0], S_pad) + tuple(t.shape[2:]), dtype=t.dtype, device=t.device)
-        p[:, :S].copy_(t)
+        B, _, H, D = t.shape
+        p = torch.empty((B, S_pad, H, D), dtype=t.dtype, device=t.device)
+        _ck(lib().ulysses_pad_seq(_p(t), _p(p), S, S_pad, B, H, D, _dtype_code(t), _stream(stream)))
         out.append(p)
-    dev = tensors[0].device
-    if cu_seqlens is None:
-        cu = torch.tensor([0, S, S_pad], dtype=torch.int32, device=dev)
-    else:
-        cu = torch.cat([cu_seqlens.to(torch.int32), torch.tensor([S_pad], dtype=torch.int32, device=dev)])
+    nd = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    cu = torch.empty(nd + 2, dtype=torch.int32, device=tensors[0].device)
+    cp, _ = _cu(cu_seqlens)
+    _ck(lib().ulysses_pad_cu_seqlens(cp, nd, _p(cu), S, S_pad, _stream(stream)))
     return out, cu, S
 
 
@@ -311,84 +363,57 @@ def selftest_wait_timeout(limit_ns=50_000_000, stream=None):
 
 # --------------------------------------------------------------- ring variant
 
-def _chunks(x_seq, P):
-    """Each rank's token chunk of a [1,S,H,D] tensor in head layout [1,H,L,D]
-    (the library's re-layout with one rank over the chunk)."""
-    L = x_seq.shape[1] // P
-    return [seq2head(x_seq[:, r * L:(r + 1) * L], 1) for r in range(P)]
+def ring_workspace(S, H_q, H_kv, D, P, dtype=BF16, device="cuda"):
+    n = lib().ulysses_ring_workspace(S, H_q, H_kv, D, P, dtype)
+    if n == 0:
+        raise UlyssesError(ERR_INVALID, "invalid ring shape")
+    return torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def ring_attention_fwd(q_seq, k_seq, v_seq, P, causal=True, scale=None, stream=None):
+def ring_attention_fwd(q_seq, k_seq, v_seq, P, causal=True, scale=None, workspace=None, stream=None):
     """Ring-attention variant of the same layer (the scheme the pages compare
-    Ulysses with), on P virtual ranks: rank r keeps query chunk r and meets KV
-    chunk (r - t) mod P at ring step t; steps whose chunk lies wholly in the
-    future are skipped under the causal mask, the diagonal step is causal and
-    the others are full.  The steps' (O, LSE) are merged with their
-    log-sum-exp weights.  Returns (O [1,S,H_q,D], LSE chunks [P,H_q,L])."""
+    Ulysses with), on P virtual ranks, run by the library's ring driver: rank
+    r keeps query chunk r and meets KV chunk (r - t) mod P at ring step t;
+    steps wholly in the future are skipped under the causal mask, the
+    diagonal step is causal and the others are full; the steps' (O, LSE) are
+    merged with their log-sum-exp weights.  Returns (O [1,S,H_q,D], LSE
+    chunks [P,H_q,L])."""
     B, S, Hq, D = q_seq.shape
     Hkv = k_seq.shape[2]
     if B != 1 or S % P:
         raise ValueError("ring variant: B == 1 and S divisible by P")
-    L, dt, st = S // P, _dtype_code(q_seq), _stream(stream)
-    qc, kc, vc = _chunks(q_seq, P), _chunks(k_seq, P), _chunks(v_seq, P)
+    dt = _dtype_code(q_seq)
+    if workspace is None:
+        workspace = ring_workspace(S, Hq, Hkv, D, P, dt, q_seq.device)
     out = torch.empty_like(q_seq)
-    lse = torch.empty((P, Hq, L), dtype=torch.float32, device=q_seq.device)
-    o_acc = torch.empty((Hq * L, D), dtype=torch.float32, device=q_seq.device)
-    oh = torch.empty_like(qc[0])
-    for r in range(P):
-        first = 1
-        for t in range(P):
-            c = (r - t) % P
-            if causal and c > r:
-                continue
-            op, lp = attn_fwd(qc[r], kc[c], vc[c], Hq, Hkv, 1, causal=causal and c == r, scale=scale,
-                              stream=stream)
-            _ck(lib().ulysses_lse_merge(_p(o_acc), _p(lse[r]), _p(op), _p(lp), Hq * L, D, dt, first, st))
-            first = 0
-        _ck(lib().ulysses_cast_f32(_p(oh), _p(o_acc), oh.numel(), dt, st))
-        head2seq(oh, out[:, r * L:(r + 1) * L], 1, stream=stream)
+    lse = torch.empty((P, Hq, S // P), dtype=torch.float32, device=q_seq.device)
+    _ck(lib().ulysses_ring_fwd(_p(q_seq), _p(k_seq), _p(v_seq), _p(out), _p(lse), S, Hq, Hkv, D, P,
+                               int(bool(causal)), float(scale or 0.0), dt, _p(workspace), workspace.numel(),
+                               _stream(stream)))
     return out, lse
 
 
-def ring_attention_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, P, causal=True, scale=None, stream=None):
-    """Backward of ring_attention_fwd: every (query chunk, KV chunk) step runs
-    the attention backward with the merged LSE and O, and the steps' partial
-    dQ, dK, dV are summed.  Returns fp32 (dQ, dK, dV) in sequence layout."""
+def ring_attention_bwd(q_seq, k_seq, v_seq, o_seq, do_seq, lse, P, causal=True, scale=None, workspace=None,
+                       stream=None):
+    """Backward of ring_attention_fwd (library ring driver): every (query
+    chunk, KV chunk) step runs the attention backward with the merged LSE and
+    O, and the steps' partial dQ, dK, dV are summed.  Returns fp32 (dQ, dK,
+    dV) in sequence layout."""
     B, S, Hq, D = q_seq.shape
     Hkv = k_seq.shape[2]
-    L, st = S // P, _stream(stream)
-    qc, kc, vc = _chunks(q_seq, P), _chunks(k_seq, P), _chunks(v_seq, P)
-    oc, doc = _chunks(o_seq, P), _chunks(do_seq, P)
+    if B != 1 or S % P:
+        raise ValueError("ring variant: B == 1 and S divisible by P")
+    dt = _dtype_code(q_seq)
     dev = q_seq.device
-    dq_acc = [None] * P
-    dk_acc = [None] * P
-    dv_acc = [None] * P
-
-    def acc(lst, i, part):
-        if lst[i] is None:
-            lst[i] = part
-        else:
-            _ck(lib().ulysses_add_f32(_p(lst[i]), _p(part), part.numel(), st))
-
-    for r in range(P):
-        for t in range(P):
-            c = (r - t) % P
-            if causal and c > r:
-                continue
-            dqp, dkp, dvp = attn_bwd(qc[r], kc[c], vc[c], oc[r], doc[r], lse[r].unsqueeze(0), Hq, Hkv, 1,
-                                     causal=causal and c == r, scale=scale, stream=stream)
-            acc(dq_acc, r, dqp)
-            acc(dk_acc, c, dkp)
-            acc(dv_acc, c, dvp)
+    if workspace is None:
+        workspace = ring_workspace(S, Hq, Hkv, D, P, dt, dev)
     dq = torch.empty(q_seq.shape, dtype=torch.float32, device=dev)
     dk = torch.empty(k_seq.shape, dtype=torch.float32, device=dev)
     dv = torch.empty(v_seq.shape, dtype=torch.float32, device=dev)
-    for r in range(P):
-        head2seq(dq_acc[r], dq[:, r * L:(r + 1) * L], 1, stream=stream)
-        head2seq(dk_acc[r], dk[:, r * L:(r + 1) * L], 1, stream=stream)
-        head2seq(dv_acc[r], dv[:, r * L:(r + 1) * L], 1, stream=stream)
+    _ck(lib().ulysses_ring_bwd(_p(q_seq), _p(k_seq), _p(v_seq), _p(o_seq), _p(do_seq), _p(lse), _p(dq), _p(dk),
+                               _p(dv), S, Hq, Hkv, D, P, int(bool(causal)), float(scale or 0.0), dt,
+                               _p(workspace), workspace.numel(), _stream(stream)))
     return dq, dk, dv
-
 
 
 # --------------------------------------------------------------- projections

@@ -9,6 +9,7 @@ import torch
 
 import oracle
 from long_context_sequence_seq_gb300 import inputs, ulysses as U
+from tests import oracle_pool
 from tests.gpu_util import LSE_TOL, TOL, f64, max_err, seq_inputs
 
 pytestmark = pytest.mark.gpu
@@ -109,28 +110,29 @@ def test_tiny_mha_fp32_workload_all_chunks():
         ref = cur
 
 
-def test_qwen3_4b_8k_two_kv_groups():
-    """S=8192, H_q=32, H_kv=8, D=128, P=4, head_chunk=8 (bf16): full oracle on
-    the kv groups of rank 0 and rank 3 (4 q heads each), all elements."""
+def test_qwen3_4b_8k_all_kv_groups():
+    """S=8192, H_q=32, H_kv=8, D=128, P=4, head_chunk=8 (bf16): the full
+    oracle on every kv group (all 32 q heads, all 8 kv heads), all elements."""
     w = inputs.WORKLOADS["qwen3_4b_8k"]
     q, k, v, do = seq_inputs(w.S, w.H_q, w.H_kv, w.D, w.dtype)
     o, lse = U.layer_fwd(q, k, v, w.P, w.head_chunk)
     dq, dk, dv = U.layer_bwd(q, k, v, o, do, lse, w.P, w.head_chunk)
     U.check()
     G = w.G
-    for g in (0, 7):      # kv head 0 (rank 0) and kv head 7 (rank 3)
-        hs = slice(g * G, (g + 1) * G)
-        Q = f64(q[0, :, hs]).transpose(1, 0, 2)
-        DO = f64(do[0, :, hs]).transpose(1, 0, 2)
-        K = f64(k[0, :, g:g + 1]).transpose(1, 0, 2)
-        V = f64(v[0, :, g:g + 1]).transpose(1, 0, 2)
-        ro, rl = oracle.attn_fwd(Q, K, V)
-        rq, rk, rv = oracle.attn_bwd(Q, K, V, DO)
-        assert max_err(f64(o[0, :, hs]).transpose(1, 0, 2), ro) <= TOL["bf16"]
-        assert max_err(f64(lse[0, hs]), rl) <= LSE_TOL["bf16"]
-        assert max_err(f64(dq[0, :, hs]).transpose(1, 0, 2), rq) <= TOL["bf16"]
-        assert max_err(f64(dk[0, :, g:g + 1]).transpose(1, 0, 2), rk) <= TOL["bf16"]
-        assert max_err(f64(dv[0, :, g:g + 1]).transpose(1, 0, 2), rv) <= TOL["bf16"]
+    f32 = lambda t: t.detach().float().cpu().numpy()  # noqa: E731
+    qn, kn, vn, don = f32(q[0]), f32(k[0]), f32(v[0]), f32(do[0])
+    jobs = [(qn[:, h], kn[:, h // G], vn[:, h // G], don[:, h], None, True) for h in range(w.H_q)]
+    res = oracle_pool.run(oracle_pool.head_fwd_bwd, jobs)
+    on, ln, dqn, dkn, dvn = f64(o[0]), f64(lse[0]), f64(dq[0]), f64(dk[0]), f64(dv[0])
+    for h, (ro, rl, rq, _, _) in enumerate(res):
+        assert max_err(on[:, h], ro) <= TOL["bf16"], (h, "O")
+        assert max_err(ln[h], rl) <= LSE_TOL["bf16"], (h, "LSE")
+        assert max_err(dqn[:, h], rq) <= TOL["bf16"], (h, "dQ")
+    for g in range(w.H_kv):
+        rk = sum(res[h][3] for h in range(g * G, (g + 1) * G))
+        rv = sum(res[h][4] for h in range(g * G, (g + 1) * G))
+        assert max_err(dkn[:, g], rk) <= TOL["bf16"], (g, "dK")
+        assert max_err(dvn[:, g], rv) <= TOL["bf16"], (g, "dV")
 
 
 def test_bad_cu_seqlens_flagged_not_faulted():

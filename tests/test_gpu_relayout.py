@@ -59,3 +59,42 @@ def test_relayout_full_64k_layer(H, C):
         h = U.seq2head(x, P, C, st)
         assert np.array_equal(_bits(h), oracle.seq2head(xb, P, C, st)), st
     U.check()
+
+
+@pytest.mark.parametrize("S,B,D,P,dtype", [(256, 1, 128, 4, "bf16"), (1000, 2, 64, 2, "bf16"),
+                                           (96, 1, 128, 2, "fp32"), (65536, 1, 128, 4, "bf16")])
+def test_batched_relayout_bit_exact(S, B, D, P, dtype):
+    """One launch for a stage's Q, K, V, O and dO (and its gradients back):
+    every tensor bit-exact against the oracle's permutation, the scatter
+    restores the sequence layout, and the accumulating form adds (fp32)."""
+    Hq, Hkv = 4 * P, 2 * P if P > 1 else 2
+    C, Ckv = Hq // P // 2, max(1, Hkv // P // 2)
+    seeds = (31, 32, 33, 34, 35)
+    hs = (Hq, Hkv, Hkv, Hq, Hq)
+    cs = (C, Ckv, Ckv, C, C)
+    xs = [inputs.device_tensor((B, S, h, D), sd, dtype) for h, sd in zip(hs, seeds)]
+    bits = [_bits(x) for x in xs]
+    n_st = P * (Hq // P // C)
+    for st in (0, n_st - 1):
+        kst = st * (Hkv // P // Ckv) // (Hq // P // C)
+        stg = (st, kst, kst, st, st)
+        outs = [torch.empty((B, c, S, D), dtype=x.dtype, device="cuda") for x, c in zip(xs, cs)]
+        U.seq2head_n([(x, o, c, s) for x, o, c, s in zip(xs, outs, cs, stg)], P)
+        for o, xb, c, s in zip(outs, bits, cs, stg):
+            assert np.array_equal(_bits(o), oracle.seq2head(xb, P, c, s)), st
+        ys = [torch.zeros_like(x) for x in xs]
+        U.head2seq_n([(o, y, c, s) for o, y, c, s in zip(outs, ys, cs, stg)], P)
+        for o, y, c, s in zip(outs, ys, cs, stg):
+            want = np.zeros_like(_bits(y))
+            oracle.head2seq(_bits(o), want, P, c, s)
+            assert np.array_equal(_bits(y), want), st
+        if dtype == "fp32":
+            base = [torch.randn_like(y) for y in ys[:3]]
+            acc = [b.clone() for b in base]
+            U.head2seq_n([(o, a, c, s, 1) for o, a, c, s in zip(outs[:3], acc, cs[:3], stg[:3])], P)
+            for o, a, b, c, s in zip(outs[:3], acc, base, cs[:3], stg[:3]):
+                want = b.cpu().numpy().copy()
+                heads = oracle.stage_heads(a.shape[2], P, c, s)
+                want[:, :, heads] += np.transpose(o.cpu().numpy(), (0, 2, 1, 3))
+                assert np.array_equal(a.cpu().numpy(), want), st
+    U.check()

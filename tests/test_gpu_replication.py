@@ -90,3 +90,24 @@ def test_padding_to_multiple_of_P(S, P, docs):
     assert max_err(f64(lse[:, :, :S])[0], rl) <= LSE_TOL["bf16"]
     for got, want in ((dq, rq), (dk, rk), (dv, rv)):
         assert max_err(f64(got[:, :S])[0], want) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("S,P,B,H,D,dtype,docs", [(10, 4, 2, 3, 64, "bf16", None), (1000, 8, 1, 2, 128, "fp32", [400, 600]),
+                                                   (17, 1, 1, 1, 128, "bf16", None), (64, 4, 1, 2, 64, "bf16", [64])])
+def test_pad_kernels_bit_exact(S, P, B, H, D, dtype, docs):
+    """ulysses_pad_seq copies every real token bit for bit and zeroes the pad
+    tokens; ulysses_pad_cu_seqlens appends the pad document."""
+    x = inputs.host_tensor((B, S, H, D), 51, dtype).cuda()
+    cu = None if docs is None else torch.from_numpy(inputs.cu_seqlens_from_lengths(docs)).cuda()
+    (xp,), cup, S0 = U.pad_to_multiple([x], P, cu)
+    U.check()
+    S_pad = U.padded_length(S, P)
+    assert S0 == S and xp.shape == (B, S_pad, H, D)
+    bits = lambda t: t.cpu().view(torch.int16 if t.element_size() == 2 else torch.int32)  # noqa: E731
+    assert torch.equal(bits(xp[:, :S]), bits(x))
+    assert torch.count_nonzero(bits(xp[:, S:])) == 0
+    real = [0, S] if docs is None else [0] + list(np.cumsum(docs))
+    if S_pad == S:
+        assert xp is x and (cup is cu)
+    else:
+        assert cup.cpu().tolist() == real + [S_pad]

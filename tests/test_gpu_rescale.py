@@ -8,9 +8,13 @@ the sequence (keys aligned with the queries and scaled up with their
 position), and spread the scores over a wide range, then compare forward and
 backward with the fp64 oracle.
 
-Tolerance: the bf16 bound of the other tests (2e-2) applied relative to the
-largest reference magnitude when that exceeds 1, since large scores give large
-gradients; LSE within 1e-3.
+Tolerance: max-abs 2e-2 (the bound of the N(0,1) workloads) plus, element by
+element, the worst-case error the bf16 operands of the second-stage MMAs can
+add (tests.gpu_util.bf16_rounding_bound: the bf16 unit roundoff 2^-8 on P and
+dS, and on the stored O that D_i is formed from).  The "wide" scores give gradients of
+magnitude 10-15, where that rounding alone exceeds 2e-2; a wrong lazy
+rescale errs by the magnitude of the result, far outside it.  LSE within
+1e-3.
 """
 import numpy as np
 import pytest
@@ -18,7 +22,7 @@ import torch
 
 import oracle
 from long_context_sequence_seq_gb300 import inputs, ulysses as U
-from tests.gpu_util import f64
+from tests.gpu_util import bf16_rounding_bound, f64
 
 pytestmark = pytest.mark.gpu
 
@@ -42,10 +46,10 @@ def _head_inputs(S, Hq, Hkv, D, mode, seed=0):
     return to(q), to(k), to(v), to(do)
 
 
-def _check(got, ref, tol):
-    scale = max(1.0, float(np.max(np.abs(ref))) if ref.size else 1.0)
-    err = float(np.max(np.abs(got - ref))) if ref.size else 0.0
-    assert err <= tol * scale, (err, scale)
+def _check(name, got, ref, bound):
+    err = np.abs(got - ref)
+    excess = err - (2e-2 + bound)
+    assert np.all(excess <= 0), (name, float(err.max()), float(excess.max()))
 
 
 @pytest.mark.parametrize("mode,S,docs", [
@@ -65,10 +69,11 @@ def test_online_softmax_stress(mode, S, docs):
     Q, K, V, DO = f64(q)[0], f64(k)[0], f64(v)[0], f64(do)[0]
     ro, rl = oracle.attn_fwd(Q, K, V, cu_np, True)
     rq, rk, rv = oracle.attn_bwd(Q, K, V, DO, cu_np, True)
-    _check(f64(o)[0], ro, 2e-2)
+    b_o, b_q, b_k, b_v = bf16_rounding_bound(Q, K, V, DO, cu_np, True)
+    _check("O", f64(o)[0], ro, b_o)
     assert float(np.max(np.abs(f64(lse)[0] - rl))) <= 1e-3
-    for got, ref in ((dq, rq), (dk, rk), (dv, rv)):
-        _check(f64(got)[0], ref, 2e-2)
+    for name, got, ref, bnd in (("dQ", dq, rq, b_q), ("dK", dk, rk, b_k), ("dV", dv, rv, b_v)):
+        _check(name, f64(got)[0], ref, bnd)
     if mode == "growing":
         # the construction does what it says: row maxima rise by far more than
         # 8 log2 units over the sequence

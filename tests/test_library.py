@@ -103,20 +103,28 @@ def test_kv_replication_validation(libpath):
     assert L.ulysses_head2seq_add(dummy, ctypes.c_void_p(1 << 20), 32, 1, 2, 128, 4, 0, 1, U.BF16, None) == U.ERR_UNSUPPORTED
 
 
-def test_pad_to_multiple_host():
-    """Padding to a multiple of P puts the pad positions in a document of
-    their own (host logic, CPU tensors)."""
-    import torch
+def test_pad_and_ring_validation(libpath):
+    """Padding and the ring driver reject bad shapes on the host."""
     from long_context_sequence_seq_gb300 import ulysses as U
-    x = torch.arange(2 * 10 * 3 * 2, dtype=torch.float32).reshape(2, 10, 3, 2)
-    (p,), cu, S = U.pad_to_multiple([x], 4)
-    assert S == 10 and p.shape == (2, 12, 3, 2)
-    assert torch.equal(p[:, :10], x) and torch.count_nonzero(p[:, 10:]) == 0
-    assert cu.tolist() == [0, 10, 12]
-    (q,), cu2, _ = U.pad_to_multiple([x[:1]], 4, torch.tensor([0, 4, 10], dtype=torch.int32))
-    assert cu2.tolist() == [0, 4, 10, 12]
-    (r,), cu3, _ = U.pad_to_multiple([x[:, :8]], 4)
-    assert r.shape[1] == 8 and cu3 is None
+    L = U.lib()
+    d = ctypes.c_void_p(1 << 20)
+    e = ctypes.c_void_p(1 << 24)
+    assert U.padded_length(10, 4) == 12 and U.padded_length(12, 4) == 12 and U.padded_length(0, 4) == 0
+    # S_pad < S, rows not a multiple of 16 bytes, in place
+    assert L.ulysses_pad_seq(d, e, 10, 8, 1, 4, 128, U.BF16, None) == U.ERR_INVALID
+    assert L.ulysses_pad_seq(d, e, 10, 12, 1, 1, 4, U.BF16, None) == U.ERR_UNSUPPORTED
+    assert L.ulysses_pad_seq(d, ctypes.c_void_p((1 << 20) + 256), 10, 12, 1, 4, 128, U.BF16, None) == U.ERR_INVALID
+    assert L.ulysses_pad_seq(d, e, 0, 0, 1, 4, 128, U.BF16, None) == U.OK
+    assert L.ulysses_pad_cu_seqlens(d, 0, e, 10, 12, None) == U.ERR_INVALID
+    assert L.ulysses_pad_cu_seqlens(None, 0, e, 10, 8, None) == U.ERR_INVALID
+    # ring: S % P, workspace size, empty input
+    assert L.ulysses_ring_workspace(1000, 4, 2, 128, 3, U.BF16) == 0
+    n = L.ulysses_ring_workspace(1024, 4, 2, 128, 4, U.BF16)
+    assert n > 0
+    args = [d] * 5
+    assert L.ulysses_ring_fwd(*args, 1000, 4, 2, 128, 3, 1, 0.0, U.BF16, d, n, None) == U.ERR_INVALID
+    assert L.ulysses_ring_fwd(*args, 1024, 4, 2, 128, 4, 1, 0.0, U.BF16, d, n - 256, None) == U.ERR_INVALID
+    assert L.ulysses_ring_fwd(*args, 0, 4, 2, 128, 4, 1, 0.0, U.BF16, d, n, None) == U.OK
 
 
 def test_selftest_wait_rejects_bad_limits(libpath):
@@ -149,3 +157,30 @@ def test_fused_layer_validation(libpath):
     assert L.ulysses_layer_fwd_fused(*args, 256, 1, 8, 8, 128, 2, 4, None, 0, 1, 0.0, U.FP32, None) == U.ERR_UNSUPPORTED
     assert L.ulysses_layer_fwd_fused(*args, 256, 1, 8, 2, 128, 4, 2, None, 0, 1, 0.0, U.BF16, None) == U.ERR_UNSUPPORTED
     assert U.lib().ulysses_layer_fused_workspace(4096, 1, 32, 8, 128, 4, 8, U.BF16) == 8 * 4096 * 4
+
+
+def test_batched_relayout_validation(libpath):
+    """ulysses_seq2head_n / head2seq_n reject bad batches on the host."""
+    from long_context_sequence_seq_gb300 import ulysses as U
+    L = U.lib()
+    It = U.RelayoutItem
+    a, b, c, d = (1 << 24), (2 << 24), (3 << 24), (4 << 24)   # 16 MiB apart, aligned
+    # S=32, B=1, D=128, P=2: Q-like (H=8, chunk 2) and K-like (H=4, chunk 1) items
+    ok = (It * 2)(It(a, b, 8, 2, 0, 0), It(c, d, 4, 1, 0, 0))
+    arr = lambda *xs: (It * len(xs))(*xs)  # noqa: E731
+    # too many items
+    many = (It * 7)(*([It(a, b, 8, 2, 0, 0)] * 7))
+    assert L.ulysses_seq2head_n(many, 7, 32, 1, 128, 2, U.BF16, None) == U.ERR_INVALID
+    # an item's destination overlapping another item's source
+    bad = arr(It(a, b, 8, 2, 0, 0), It(b + 256, d, 4, 1, 0, 0))
+    assert L.ulysses_seq2head_n(bad, 2, 32, 1, 128, 2, U.BF16, None) == U.ERR_INVALID
+    assert b"overlaps source" in L.ulysses_last_error()
+    # accumulation is a scatter-only, fp32-only option
+    add = arr(It(a, b, 8, 2, 0, 1))
+    assert L.ulysses_seq2head_n(add, 1, 32, 1, 128, 2, U.FP32, None) == U.ERR_UNSUPPORTED
+    assert L.ulysses_head2seq_n(add, 1, 32, 1, 128, 2, U.BF16, None) == U.ERR_UNSUPPORTED
+    # per-item shape rules still apply (chunk 3 does not divide 8/2 heads)
+    assert L.ulysses_seq2head_n(arr(It(a, b, 8, 3, 0, 0)), 1, 32, 1, 128, 2, U.BF16, None) == U.ERR_INVALID
+    # empty input and an empty batch are no-ops
+    assert L.ulysses_seq2head_n(ok, 2, 0, 1, 128, 2, U.BF16, None) == U.OK
+    assert L.ulysses_head2seq_n(ok, 0, 32, 1, 128, 2, U.BF16, None) == U.OK
