@@ -64,7 +64,8 @@ enum {
   ULYSSES_ERR_UNSUPPORTED = 2,
   ULYSSES_ERR_CUDA = 3,
   ULYSSES_ERR_TIMEOUT = 4,
-  ULYSSES_ERR_BAD_SEQLENS = 5
+  ULYSSES_ERR_BAD_SEQLENS = 5,
+  ULYSSES_ERR_BOUNDS = 6
 };
 
 enum { ULYSSES_BF16 = 0, ULYSSES_FP32 = 1 };
@@ -344,11 +345,17 @@ int ulysses_layer_bwd(const void* q_seq, const void* k_seq, const void* v_seq, c
  * ulysses_set_kernel: ULYSSES_KERNEL_AUTO or ULYSSES_KERNEL_SIMT (process wide).
  * ulysses_launch_count: number of kernels this library has launched so far in
  *   this process (host-side counter).
+ * ulysses_checked_build: 1 for the bounds-checked build of the library
+ *   (compiled with -DULYSSES_CHECKS), 0 otherwise.  In the checked build every
+ *   kernel checks its global-memory indexes against the sizes of the buffers
+ *   it was given; a failed check skips the access and ulysses_check returns
+ *   ULYSSES_ERR_BOUNDS.  The normal build compiles the checks away.
  * ------------------------------------------------------------------------- */
 int ulysses_check(void* stream);
 const char* ulysses_last_error(void);
 int ulysses_set_kernel(int which);
 long long ulysses_launch_count(void);
+int ulysses_checked_build(void);
 
 #ifdef __cplusplus
 }

@@ -19,6 +19,12 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libulysses.so")
+# The bounds-checked variant (-DULYSSES_CHECKS): every kernel checks its
+# global-memory indexes against the buffers' sizes, records a failed check in
+# the device error word (ulysses_check returns ULYSSES_ERR_BOUNDS) and skips
+# the access.  Same ABI; loaded instead of LIB when ULYSSES_CHECKED=1.
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libulysses_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -43,19 +49,21 @@ def _stale(lib: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra=None) -> str:
+def build(force: bool = False, verbose: bool = False, extra=None, checked: bool = False) -> str:
     srcs = sources()
+    lib_path = LIB_CHECKED if checked else LIB
+    build_dir = BUILD_CHECKED if checked else BUILD
     deps = srcs + [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     deps.append(os.path.join(INCLUDE, "ulysses.h"))
     deps.append(os.path.abspath(__file__))
-    if not force and not _stale(LIB, deps):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    if not force and not _stale(lib_path, deps):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    extra = list(extra or [])
+    extra = list(extra or []) + (["-DULYSSES_CHECKS"] if checked else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -66,15 +74,15 @@ def build(force: bool = False, verbose: bool = False, extra=None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-ldl", "-lpthread", "-lrt"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra=["-Xptxas", "-v"] if "--ptxas" in sys.argv else None))
+                extra=["-Xptxas", "-v"] if "--ptxas" in sys.argv else None, checked="--checked" in sys.argv))

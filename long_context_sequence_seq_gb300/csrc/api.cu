@@ -841,6 +841,7 @@ int ulysses_check(void* stream) {
   if (e != cudaSuccess) return set_error(ULYSSES_ERR_CUDA, "error-word read failed: %s", cudaGetErrorString(e));
   if (w & kErrTimeout) return set_error(ULYSSES_ERR_TIMEOUT, "a kernel gave up a bounded wait");
   if (w & kErrSeqlens) return set_error(ULYSSES_ERR_BAD_SEQLENS, "cu_seqlens must rise from 0 to S");
+  if (w & kErrBounds) return set_error(ULYSSES_ERR_BOUNDS, "a kernel index fell outside its buffer (checked build)");
   return ULYSSES_OK;
 }
 
@@ -854,5 +855,13 @@ int ulysses_set_kernel(int which) {
 }
 
 long long ulysses_launch_count(void) { return g_launches.load(); }
+
+int ulysses_checked_build(void) {
+#ifdef ULYSSES_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
+}
 
 }  // extern "C"

@@ -123,8 +123,12 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(
     if (i >= S) continue;
     const float inv = 1.f / l[r];
 #pragma unroll
-    for (int dd = 0; dd < DW; ++dd) o[(n * S + i) * D + lane + 32 * dd] = from_f32<T>(acc[r][dd] * inv);
-    if (lane == 0) lse[lse_index(n, nq, lse_bstride, S, i)] = m[r] + logf(l[r]);
+    for (int dd = 0; dd < DW; ++dd) {
+      const int64_t oi = (n * S + i) * D + lane + 32 * dd;
+      if (in_bounds(oi, (int64_t)gridDim.y * S * D)) o[oi] = from_f32<T>(acc[r][dd] * inv);
+    }
+    const int64_t li = lse_index(n, nq, lse_bstride, S, i);
+    if (lane == 0 && in_bounds(li, ((int64_t)gridDim.y + nq - 1) / nq * lse_bstride)) lse[li] = m[r] + logf(l[r]);
   }
 }
 
@@ -138,7 +142,8 @@ __global__ void __launch_bounds__(256) bwd_delta_kernel(const T* __restrict__ o,
   if (row >= rows) return;
   float s = 0.f;
 #pragma unroll
-  for (int d = lane; d < D; d += 32) s = fmaf(to_f32<T>(o[row * D + d]), to_f32<T>(dO[row * D + d]), s);
+  if (in_bounds(row * D + D - 1, rows * D))
+    for (int d = lane; d < D; d += 32) s = fmaf(to_f32<T>(o[row * D + d]), to_f32<T>(dO[row * D + d]), s);
   s = warp_sum(s);
   if (lane == 0) delta[row] = s;
 }
@@ -168,8 +173,9 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_dq_kernel(
     int64_t i = row0 + warp * kRowsPerWarp + r;
     if (i < S) {
       key_range(cu, nd, S, causal, i, lo[r], hi[r]);
-      L[r] = lse[lse_index(n, nq, lse_bstride, S, i)];
-      Dl[r] = delta[n * S + i];
+      const int64_t li = lse_index(n, nq, lse_bstride, S, i), di = n * S + i;
+      L[r] = in_bounds(li, ((int64_t)gridDim.y + nq - 1) / nq * lse_bstride) ? lse[li] : 0.f;
+      Dl[r] = in_bounds(di, (int64_t)gridDim.y * S) ? delta[di] : 0.f;
     } else { lo[r] = 0; hi[r] = 0; L[r] = 0.f; Dl[r] = 0.f; }
 #pragma unroll
     for (int dd = 0; dd < DW; ++dd) acc[r][dd] = 0.f;
@@ -211,7 +217,10 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_dq_kernel(
     int64_t i = row0 + warp * kRowsPerWarp + r;
     if (i >= S) continue;
 #pragma unroll
-    for (int dd = 0; dd < DW; ++dd) dq[(n * S + i) * D + lane + 32 * dd] = acc[r][dd] * scale;
+    for (int dd = 0; dd < DW; ++dd) {
+      const int64_t qi = (n * S + i) * D + lane + 32 * dd;
+      if (in_bounds(qi, (int64_t)gridDim.y * S * D)) dq[qi] = acc[r][dd] * scale;
+    }
   }
 }
 
@@ -256,8 +265,10 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_dkdv_kernel(
       load_rows<T, D>(&dOs[0][0], D + 1, dO + n * S * D, S, c0, kChunk);
       if (threadIdx.x < kChunk) {
         int64_t i = c0 + threadIdx.x;
-        Ls[threadIdx.x] = i < S ? lse[lse_index(n, nq, lse_bstride, S, i)] : 0.f;
-        Ds[threadIdx.x] = i < S ? delta[n * S + i] : 0.f;
+        const int64_t li = lse_index(n, nq, lse_bstride, S, i), di = n * S + i;
+        const int64_t n_q = (int64_t)gridDim.y * G;   // this kernel's grid runs over kv heads
+        Ls[threadIdx.x] = (i < S && in_bounds(li, (n_q + nq - 1) / nq * lse_bstride)) ? lse[li] : 0.f;
+        Ds[threadIdx.x] = (i < S && in_bounds(di, n_q * S)) ? delta[di] : 0.f;
       }
       __syncthreads();
       const int64_t i = c0 + lane;
@@ -293,8 +304,10 @@ __global__ void __launch_bounds__(kWarps * 32) simt_bwd_dkdv_kernel(
     if (j >= S) continue;
 #pragma unroll
     for (int dd = 0; dd < DW; ++dd) {
-      dk[(kvh * S + j) * D + lane + 32 * dd] = ak[r][dd] * scale;
-      dv[(kvh * S + j) * D + lane + 32 * dd] = av[r][dd];
+      const int64_t ki = (kvh * S + j) * D + lane + 32 * dd;
+      if (!in_bounds(ki, (int64_t)gridDim.y * S * D)) continue;
+      dk[ki] = ak[r][dd] * scale;
+      dv[ki] = av[r][dd];
     }
   }
 }

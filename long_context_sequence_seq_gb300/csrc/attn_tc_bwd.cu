@@ -14,15 +14,18 @@
 // its block (accumulated in TMEM, no atomics) and walks the G query heads and
 // every 64-row query block that can see its keys.  Transposed formulation,
 // so the key index is the TMEM lane:
-//   S^T  = K Q_i^T            (M=128 keys, N=64 queries, K=D)
-//   dP^T = V dO_i^T
-//   softmax warps: P^T = exp2(S^T*scale*log2e - LSE_i*log2e), masked;
-//                  dS^T = P^T (dP^T - D_i); both stored back to TMEM as bf16,
-//                  dS^T also to shared memory (swizzled, [key][query]).
+//   S^T  = K Q_i^T            (M=128 keys, N=64 queries, K=D; A = K from smem)
+//   dP^T = V dO_i^T           (A = V, copied into TMEM once per CTA)
+//   softmax warps: P^T = exp2(S^T*scale*log2e - LSE_i*log2e), masked, stored
+//                  back to TMEM as bf16; dS^T = P^T (dP^T - D_i) to shared
+//                  memory (swizzled, [key][query]).
 //   dV  += P^T dO_i            (A = P^T from TMEM, B = dO_i, MN-major)
-//   dK  += dS^T Q_i            (A = dS^T from TMEM, B = Q_i, MN-major)
+//   dK  += dS^T Q_i            (A = dS^T from shared memory, K-major; B = Q_i, MN-major)
 //   dQ_i^T = K^T dS^T          (M = D, N = 64 queries; A = K, MN-major;
 //                               B = dS^T from shared memory, MN-major)
+// Keeping V in TMEM makes dP^T an A-from-TMEM MMA (the shared-memory operand
+// reads bound the N = 64 shared-memory form) and frees V's 32 KB of shared
+// memory for a fifth Q/dO stage.
 // Four readout warps then read dQ_i^T out of TMEM (lane = feature d) and
 // write scale * dQ_i as [query][feature] fp32 rows into the tile's consumed
 // Q/dO stage buffers; a flusher warp adds them into dQ with TMA bulk
@@ -35,8 +38,8 @@
 // two per lane quarter, each taking 32 of the tile's 64 queries (thread = key
 // row).  Warpgroups 0-1 run on 112 registers per thread and give the rest to
 // the gradient warpgroups (144).  TMEM columns: dV [0,128), dK [128,256), two
-// S^T/P^T buffers [256,384) that also receive each tile's dQ^T, two
-// dP^T/dS^T buffers [384,512).
+// S^T/P^T buffers [256,384) that also receive each tile's dQ^T, one dP^T
+// buffer [384,448) and V [448,512) (bf16, two features per column).
 #include <type_traits>
 
 #include "internal.h"
@@ -53,7 +56,7 @@ using namespace tc;
 constexpr int BN = 128;     // keys per CTA
 constexpr int BMQ = 64;     // queries per inner tile
 constexpr int D = 128;
-constexpr int NSTAGE = 4;   // Q/dO/LSE/D_i ring (a consumed stage also stages its dQ tile)
+constexpr int NSTAGE = 5;   // Q/dO/LSE/D_i ring (a consumed stage also stages its dQ tile)
 constexpr int kThreads = 512;
 constexpr int kReadWarps = 4;   // warps 4..7: dQ^T readout, one per TMEM lane quarter
 constexpr int kGradWarps = 8;   // warps 8..15: two per TMEM lane quarter, one per 32-query half
@@ -63,8 +66,8 @@ constexpr uint32_t kRegsLow = 112, kRegsHigh = 144;
 static_assert(2 * 128 * kRegsLow + 2 * 128 * kRegsHigh == 128 * kThreads, "register split");
 constexpr uint32_t kTmemCols = 512;
 // TMEM: dV, dK accumulators; two S^T/P^T buffers (each later reused for the
-// tile's dQ^T); two dP^T/dS^T buffers.
-constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384;
+// tile's dQ^T); one dP^T buffer; V as the A operand of dP^T.
+constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 384, kColV = 448;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // TMEM column of bf16 K-step kk (16 queries) of a packed P^T / dS^T tile: each
@@ -79,19 +82,20 @@ struct BwdLayout {
   static constexpr int kTileQ = kChunkQ * (D / 64);
   static constexpr int kTileDS = BN * BMQ * 2;       // [128 keys][64 queries] bf16
   static constexpr int kK = 0;
-  static constexpr int kV = kK + kTileKV;
-  static constexpr int kQ = kV + kTileKV;                    // NSTAGE tiles
+  static constexpr int kQ = kK + kTileKV;                    // NSTAGE tiles
   static constexpr int kDO = kQ + NSTAGE * kTileQ;            // NSTAGE tiles
   static constexpr int kDS = kDO + NSTAGE * kTileQ;           // one dS^T tile
   static constexpr int kStat = kDS + kTileDS;                 // NSTAGE x {LSE2[64], D[64]}
   static constexpr int kBar = kStat + NSTAGE * 2 * BMQ * 4;
   // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[2], ds_full[2], dsm_free,
-  // dq_full[2], dq_empty, fin, drain, stg_full[NSTAGE], dk_done[NSTAGE]
-  static constexpr int kNumBar = 1 + 4 * NSTAGE + 7 + 3;
+  // dq_full[2], dq_empty, fin, drain, stg_full[NSTAGE], dk_done[NSTAGE],
+  // v_full, dp_free
+  static constexpr int kNumBar = 1 + 4 * NSTAGE + 7 + 3 + 2;
   static constexpr int kMisc = kBar + kNumBar * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
+static_assert(BwdLayout::kAlloc <= 232448, "shared memory budget");
 
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __restrict__ o,
                                                       const __nv_bfloat16* __restrict__ dO,
@@ -103,6 +107,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   if (hr >= rows) return;
   // where the row lives: head layout [n][S][D], or sequence layout [S][hq_tot][D]
   const int64_t row = seq ? (hr % S) * hq_tot + hr / S : hr;
+  if (!in_bounds(row * D + D - 1, (seq ? (int64_t)hq_tot * S : rows) * D)) return;
   // 128 features = 32 lanes x 4
   const uint2 ov = *reinterpret_cast<const uint2*>(o + row * D + lane * 4);
   const uint2 dv = *reinterpret_cast<const uint2*>(dO + row * D + lane * 4);
@@ -141,13 +146,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                   float* __restrict__ dq, float* __restrict__ dk, float* __restrict__ dv,
                   int64_t S, int nq, int G, int64_t lse_bstride, const int32_t* __restrict__ cu,
                   int nd, int causal, float scale, const __grid_constant__ CUtensorMap tmDQ, int seq,
-                  int hkv_tot) {
+                  int hkv_tot, const __nv_bfloat16* __restrict__ vptr) {
   using L = BwdLayout;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* sK = smem + L::kK;
-  uint8_t* sV = smem + L::kV;
   uint8_t* sQ = smem + L::kQ;
   uint8_t* sDO = smem + L::kDO;
   uint8_t* sDS = smem + L::kDS;
@@ -165,6 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* drain = fin + 1;
   uint64_t* stg_full = drain + 1;     // dQ tile of a stage written to its Q/dO buffers
   uint64_t* dk_done = stg_full + NSTAGE;   // dK of a stage's tile done: its Q buffer is free
+  uint64_t* v_full = dk_done + NSTAGE;     // V copied into TMEM
+  uint64_t* dp_free = v_full + 1;          // every gradient warp has read the tile's dP^T
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -189,11 +195,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dsm_free, 1);
     mbar_init(fin, 1);
     mbar_init(drain, 1);
+    mbar_init(v_full, kReadWarps);
+    mbar_init(dp_free, kGradWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch(&tmQ); tma_prefetch(&tmK); tma_prefetch(&tmV); tma_prefetch(&tmDO);
+    tma_prefetch(&tmQ); tma_prefetch(&tmK); tma_prefetch(&tmDO);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -218,11 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_expect_tx(kv_full, 2 * L::kTileKV);
+      mbar_expect_tx(kv_full, L::kTileKV);
       for (int c = 0; c < D / 64; ++c) {
         // head layout: (feature, row, head); sequence layout: (feature, head, row)
         tma_load_3d(sK + c * L::kChunkKV, &tmK, c * 64, seq ? kvh : (int)k0, seq ? (int)k0 : kvh, kv_full);
-        tma_load_3d(sV + c * L::kChunkKV, &tmV, c * 64, seq ? kvh : (int)k0, seq ? (int)k0 : kvh, kv_full);
       }
       for (int it = 0; it < n_it; ++it) {
         const int st = it % NSTAGE;
@@ -250,8 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int r = lane; r < BMQ; r += 32) {
         const int64_t i = q0 + r;
-        stat[r] = i < S ? lse[lse_index(n, nq, lse_bstride, S, i)] * kLog2e : 0.f;
-        stat[BMQ + r] = i < S ? delta[(int64_t)n * S + i] : 0.f;
+        const int64_t li = lse_index(n, nq, lse_bstride, S, i), di = (int64_t)n * S + i;
+        const int64_t n_q = (int64_t)gridDim.x * G;
+        stat[r] = (i < S && in_bounds(li, (n_q + nq - 1) / nq * lse_bstride)) ? lse[li] * kLog2e : 0.f;
+        stat[BMQ + r] = (i < S && in_bounds(di, n_q * S)) ? delta[di] : 0.f;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_full[st]);
@@ -261,16 +270,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t id_s = idesc_bf16(BN, BMQ, false, false);    // S^T, dP^T
     constexpr uint32_t id_g = idesc_bf16(BN, D, false, true);       // dV, dK
     constexpr uint32_t id_q = idesc_bf16(D, BMQ, true, true);       // dQ^T
-    const uint32_t k_addr = smem_u32(sK), v_addr = smem_u32(sV);
+    const uint32_t k_addr = smem_u32(sK);
     const uint64_t kd_k = sdesc_sw128(k_addr, 16, 1024);           // K, K-major
-    const uint64_t vd_k = sdesc_sw128(v_addr, 16, 1024);           // V, K-major
     const uint64_t kd_mn = sdesc_sw128(k_addr, L::kChunkKV, 1024);  // K^T, MN-major
+    const uint64_t dsd_k = sdesc_sw128(smem_u32(sDS), 16, 1024);    // dS^T as the K-major A of dK
     auto issue_scores = [&](int it) -> bool {
       const int st = it % NSTAGE;
       const uint32_t round = it / NSTAGE;
       if (!mbar_wait_warp(&q_full[st], round & 1, abort_flag)) return false;
       // S buffer of this parity held dQ^T_{it-2}: its readout must be done
       if (it >= 2 && !mbar_wait_warp(dq_empty, (it - 2) & 1, abort_flag)) return false;
+      // the single dP^T buffer: every gradient warp has read dP^T_{it-1}
+      if (it >= 1 && !mbar_wait_warp(dp_free, (it - 1) & 1, abort_flag)) return false;
       tc_fence_after();
       {
         const uint64_t qd = sdesc_sw128(smem_u32(sQ + st * L::kTileQ), 16, 1024);
@@ -282,14 +293,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off_kv = (kk >> 2) * L::kChunkKV + (kk & 3) * 32;
           const uint32_t off_q = (kk >> 2) * L::kChunkQ + (kk & 3) * 32;
           mma_ss_w(tbase + kColS + b * BMQ, sdesc_add(kd_k, off_kv), sdesc_add(qd, off_q), id_s, kk > 0 ? 1u : 0u);
-          mma_ss_w(tbase + kColDP + b * BMQ, sdesc_add(vd_k, off_kv), sdesc_add(dod, off_q), id_s, kk > 0 ? 1u : 0u);
+          // A = V from TMEM: 16 features of every key = 8 columns
+          mma_ts_w(tbase + kColDP, tbase + kColV + kk * 8, sdesc_add(dod, off_q), id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit_w(&s_full[b]);
       }
       __syncwarp();
       return true;
     };
-    bool ok = mbar_wait_warp(kv_full, 0, abort_flag);
+    bool ok = mbar_wait_warp(kv_full, 0, abort_flag) && mbar_wait_warp(v_full, 0, abort_flag);
     if (ok && n_it > 0) ok = issue_scores(0);
     for (int it = 0; ok && it < n_it; ++it) {
       if (it + 1 < n_it && !issue_scores(it + 1)) { ok = false; break; }
@@ -305,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t dsd = sdesc_sw128(smem_u32(sDS), 8192, 1024);
         // dV first (it reads P^T from S buffer b), then dQ^T into S buffer b, then
         // dK: the dQ^T readout overlaps dK, so the next scores into buffer b
-        // wait less.
+        // wait less.  dK reads the dS^T tile in shared memory (K-major A).
 #pragma unroll
         for (int kk = 0; kk < BMQ / 16; ++kk)
           mma_ts_w(tbase + kColDV, tbase + kColS + b * BMQ + packed_col(kk), sdesc_add(dod, kk * 2048), id_g,
@@ -317,11 +329,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss_w(tbase + kColS + b * BMQ, sdesc_add(kd_mn, kk * 2048), sdesc_add(dsd, kk * 2048), id_q,
                    kk > 0 ? 1u : 0u);
         mma_commit_w(&dq_full[b]);
-        mma_commit_w(dsm_free);
 #pragma unroll
         for (int kk = 0; kk < BMQ / 16; ++kk)
-          mma_ts_w(tbase + kColDK, tbase + kColDP + b * BMQ + packed_col(kk), sdesc_add(qd, kk * 2048), id_g,
+          mma_ss_w(tbase + kColDK, sdesc_add(dsd_k, kk * 32), sdesc_add(qd, kk * 2048), id_g,
                    (it > 0 || kk > 0) ? 1u : 0u);
+        mma_commit_w(dsm_free);
         mma_commit_w(&dk_done[st]);
       }
       __syncwarp();
@@ -341,7 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = kvh * G + x / n_qb;
         const int64_t q0 = q_lo + (int64_t)(x % n_qb) * BMQ;
         const int64_t rows = S - q0 < BMQ ? S - q0 : BMQ;
-        if (seq) {
+        const int64_t n_q = (int64_t)gridDim.x * G;
+        if (!in_bounds(q0, S) || (!seq && !in_bounds(((int64_t)n * S + q0 + rows) * D - 1, n_q * S * D))) {
+          // checked build only: skip the reduce, keep the pipeline going
+        } else if (seq) {
           // rows of one head are H_q D apart in the sequence layout: tensor
           // reduce-adds of 32-row boxes (rows past S are dropped)
           tma_reduce_add_3d(&tmDQ, sQ + st * L::kTileQ, 0, n, (int)q0);
@@ -374,6 +389,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;
     const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
     const int d = wq * 32 + lane;
+    {
+      // V of this CTA's keys into TMEM columns [kColV, kColV + 64): thread =
+      // key row (TMEM lane), column c = features 2c, 2c+1 (the row's bytes as
+      // 32-bit words); rows past S are zero
+      const int64_t jv = k0 + wq * 32 + lane;
+      const int64_t vrow = seq ? jv * hkv_tot + kvh : (int64_t)kvh * S + jv;
+      const bool have = jv < S && in_bounds(vrow * D + D - 1, (seq ? (int64_t)hkv_tot : (int64_t)gridDim.x) * S * D);
+      const uint4* src = reinterpret_cast<const uint4*>(vptr + (have ? vrow : 0) * D);
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {     // 64 features (32 columns) at a time
+        uint32_t w[32];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint4 a = have ? src[8 * half + e] : make_uint4(0u, 0u, 0u, 0u);
+          w[4 * e] = a.x; w[4 * e + 1] = a.y; w[4 * e + 2] = a.z; w[4 * e + 3] = a.w;
+        }
+        tmem_st32(tbase + lane_off + kColV + half * 32, w);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(v_full);
+    }
     for (int x = 0; x < n_it; ++x) {
       const uint32_t bx = (uint32_t)(x & 1);
       const int sx = x % NSTAGE;
@@ -431,10 +469,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int chi = dhi <= 0 ? 0 : (dhi >= 32 ? 32 : (int)dhi);
       uint32_t sv[32], pv[32];
       tmem_ld32(tbase + lane_off + kColS + b * BMQ + h * 32, sv);
-      tmem_ld32(tbase + lane_off + kColDP + b * BMQ + h * 32, pv);
+      tmem_ld32(tbase + lane_off + kColDP + h * 32, pv);
       tmem_ld_wait();
       reg_fence(sv);
       reg_fence(pv);
+      // dP^T is in registers: the next tile's dP^T may overwrite its buffer
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dp_free);
       uint32_t pp[16], dd[16];
       // P^T = 2^(s * scale * log2 e - LSE_i log2 e), dS^T = P^T (dP^T - D_i).
       // The mask test sits outside the loop so each version is one basic block
@@ -465,8 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         grad_cols(std::true_type{});
       // bf16 pairs: 16 columns per half, inside the half's own 32 columns
       tmem_st16(tbase + lane_off + kColS + b * BMQ + h * 32, pp);
-      tmem_st16(tbase + lane_off + kColDP + b * BMQ + h * 32, dd);
-      // the dS^T tile in shared memory was last read by dQ^T_{it-1}
+      // the dS^T tile in shared memory was last read by dQ^T_{it-1} and dK_{it-1}
       if (it >= 1 && !mbar_wait_warp(dsm_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
       uint8_t* row = sDS + jr * 128;
 #pragma unroll
@@ -493,7 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tbase + lane_off + col0 + c * 32, r);
         tmem_ld_wait();
         reg_fence(r);
-        if (j < S) {
+        const int64_t kv_elems = (seq ? (int64_t)hkv_tot : (int64_t)gridDim.x) * S * D;
+        if (j < S && in_bounds((dst - (h == 0 ? dv : dk)) + c * 32 + 31, kv_elems)) {
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(dst + c * 32 + e) =
@@ -550,7 +592,7 @@ int launch_tc_bwd(const AttnArgs& a, cudaStream_t st) {
   dim3 grid((unsigned)n_kv, (unsigned)((a.S + BN - 1) / BN));
   tc_bwd_kernel<<<grid, kThreads, smem, st>>>(tq, tk, tv, tdo, a.lse_in, a.delta, a.dq, a.dk, a.dv,
                                               a.S, a.nq, a.G, a.lse_bstride, a.cu, a.nd, a.causal,
-                                              a.scale, tdq, a.seq, a.hkv_tot);
+                                              a.scale, tdq, a.seq, a.hkv_tot, (const __nv_bfloat16*)a.v);
   count_launch();
   return check_launch("tc_bwd");
 }

@@ -324,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tbase + lane_off + kColO + c * 32, ov);
         tmem_ld_wait();
         reg_fence(ov);
-        if (valid) {
-          const int64_t row = seq ? (int64_t)i * hq_tot + n : (int64_t)n * S + i;
+        const int64_t row = seq ? (int64_t)i * hq_tot + n : (int64_t)n * S + i;
+        if (valid && in_bounds(row * D + c * 32 + 31, (seq ? (int64_t)hq_tot : (int64_t)gridDim.x) * S * D)) {
           uint4* dst = reinterpret_cast<uint4*>(out + row * D + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -338,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (valid) lse[lse_index(n, nq, lse_bstride, S, i)] = (m + __log2f(l)) * kLn2;
+      const int64_t li = lse_index(n, nq, lse_bstride, S, i);
+      if (valid && in_bounds(li, ((int64_t)gridDim.x + nq - 1) / nq * lse_bstride)) lse[li] = (m + __log2f(l)) * kLn2;
     }
   }
   // warps 2-3 have no role in this version

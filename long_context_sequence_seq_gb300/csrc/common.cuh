@@ -13,6 +13,7 @@ namespace ulysses {
 enum : unsigned {
   kErrTimeout = 1u,     // a bounded wait gave up
   kErrSeqlens = 2u,     // cu_seqlens not monotone from 0 to S
+  kErrBounds = 4u,      // checked build: an index fell outside its buffer
 };
 
 // One error word per translation unit (no relocatable device code is needed);
@@ -36,6 +37,21 @@ int set_error(int code, const char* fmt, ...);
 int check_launch(const char* what);
 
 __device__ __forceinline__ void raise_error(unsigned bits) { atomicOr(&g_error_word, bits); }
+
+// Bounds check of a global-memory index against its buffer's element count.
+// Built with -DULYSSES_CHECKS (the checked library), a failing check records
+// kErrBounds in the error word and the caller skips the access, so an index
+// bug is reported by ulysses_check instead of reading or writing outside the
+// buffer.  In the normal build it is constant true and costs nothing.
+#ifdef ULYSSES_CHECKS
+__device__ __forceinline__ bool in_bounds(int64_t i, int64_t n) {
+  if (i >= 0 && i < n) return true;
+  raise_error(kErrBounds);
+  return false;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(int64_t, int64_t) { return true; }
+#endif
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;

@@ -21,7 +21,8 @@ __global__ void __launch_bounds__(256) pad_seq_kernel(const int4* __restrict__ s
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
     const int64_t w = i % W, row = i / W;          // row = b * S_pad + t
     const int64_t t = row % S_pad, b = row / S_pad;
-    dst[i] = t < S ? src[(b * S + t) * W + w] : make_int4(0, 0, 0, 0);
+    const int64_t si = (b * S + t) * W + w;
+    dst[i] = (t < S && in_bounds(si, (total / S_pad) * S * W)) ? src[si] : make_int4(0, 0, 0, 0);
   }
 }
 

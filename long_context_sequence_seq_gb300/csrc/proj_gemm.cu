@@ -168,11 +168,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[b]);
         }
-        if (m < M) {
-          const int n = n0 + c * 32;
-          __nv_bfloat16* dst = c_head_dim > 0
-              ? out + ((int64_t)(n / c_head_dim) * M + m) * c_head_dim + (n % c_head_dim)
-              : out + m * (int64_t)N + n;
+        const int n = n0 + c * 32;
+        __nv_bfloat16* dst = c_head_dim > 0
+            ? out + ((int64_t)(n / c_head_dim) * M + m) * c_head_dim + (n % c_head_dim)
+            : out + m * (int64_t)N + n;
+        if (m < M && in_bounds((dst - out) + 31, M * (int64_t)N)) {
           uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
           for (int e = 0; e < 4; ++e)

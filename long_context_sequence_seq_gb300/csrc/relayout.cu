@@ -62,20 +62,26 @@ __global__ void __launch_bounds__(kThreads) relayout_kernel(const __grid_constan
   const int64_t head_base = (int64_t)bh * S * V;
   const int64_t seq_base = ((int64_t)b * S * jb.H + jb.h0 + hh) * V;
   const int64_t seq_step = (int64_t)jb.H * V;
+  const int64_t head_total = (int64_t)bt.B * jb.n * S * V, seq_total = (int64_t)bt.B * S * jb.H * V;
+  const int64_t src_total = kToHead ? seq_total : head_total, dst_total = kToHead ? head_total : seq_total;
   const int rows_per_blk = blockDim.y * kRows;
   for (int64_t tb = blockIdx.y; tb * rows_per_blk < S; tb += gridDim.y) {
     const int64_t t0 = tb * rows_per_blk + threadIdx.y;
     for (int v = threadIdx.x; v < V; v += blockDim.x) {
       int4 val[kRows];
+      bool ok[kRows];
 #pragma unroll
       for (int u = 0; u < kRows; ++u) {
         const int64_t t = t0 + (int64_t)u * blockDim.y;
-        if (t < S) val[u] = ld_stream(src + (kToHead ? seq_base + t * seq_step : head_base + t * V) + v);
+        const int64_t si = (kToHead ? seq_base + t * seq_step : head_base + t * V) + v;
+        const int64_t di = (kToHead ? head_base + t * V : seq_base + t * seq_step) + v;
+        ok[u] = t < S && in_bounds(si, src_total) && in_bounds(di, dst_total);
+        if (ok[u]) val[u] = ld_stream(src + si);
       }
 #pragma unroll
       for (int u = 0; u < kRows; ++u) {
-        const int64_t t = t0 + (int64_t)u * blockDim.y;
-        if (t < S) {
+        if (ok[u]) {
+          const int64_t t = t0 + (int64_t)u * blockDim.y;
           int4* p = dst + (kToHead ? head_base + t * V : seq_base + t * seq_step) + v;
           if (!kToHead && jb.add) *p = add_f32x4(*p, val[u]);
           else *p = val[u];

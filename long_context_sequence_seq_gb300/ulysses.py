@@ -16,9 +16,11 @@ import os
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libulysses.so")
+# ULYSSES_CHECKED=1 loads the bounds-checked build of the same library
+LIB_PATH = os.path.join(_PKG, "libulysses_checked.so" if os.environ.get("ULYSSES_CHECKED") == "1"
+                        else "libulysses.so")
 
-OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_SEQLENS = range(6)
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT, ERR_BAD_SEQLENS, ERR_BOUNDS = range(7)
 BF16, FP32 = 0, 1
 KERNEL_AUTO, KERNEL_SIMT = 0, 1
 
@@ -44,7 +46,8 @@ def lib():
         return _lib
     if not os.path.exists(LIB_PATH):
         raise RuntimeError(f"{LIB_PATH} is missing: build it with "
-                           "long_context_sequence_seq_gb300.build.build()")
+                           "long_context_sequence_seq_gb300.build.build() (checked=True for the "
+                           "bounds-checked variant)")
     L = ctypes.CDLL(LIB_PATH)
     vp, i64, i32, f32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     L.ulysses_seq2head.argtypes = [vp, vp, i64, i32, i32, i32, i32, i32, i32, i32, vp]
@@ -89,6 +92,7 @@ def lib():
     L.ulysses_last_error.restype = ctypes.c_char_p
     L.ulysses_set_kernel.argtypes = [i32]
     L.ulysses_launch_count.restype = ctypes.c_longlong
+    L.ulysses_checked_build.restype = ctypes.c_int
     _lib = L
     return L
 

@@ -184,3 +184,21 @@ def test_batched_relayout_validation(libpath):
     # empty input and an empty batch are no-ops
     assert L.ulysses_seq2head_n(ok, 2, 0, 1, 128, 2, U.BF16, None) == U.OK
     assert L.ulysses_head2seq_n(ok, 0, 32, 1, 128, 2, U.BF16, None) == U.OK
+
+
+def test_checked_variant_builds_and_loads():
+    """The bounds-checked library exports the same symbols and says so."""
+    import subprocess
+    import sys
+    path = B.build(checked=True)
+    lib = ctypes.CDLL(path)
+    for n in _declared():
+        assert hasattr(lib, n), n
+    assert lib.ulysses_checked_build() == 1
+    assert ctypes.CDLL(B.build()).ulysses_checked_build() == 0
+    # ULYSSES_CHECKED=1 makes the binding load it (in a fresh process)
+    code = ("from long_context_sequence_seq_gb300 import ulysses as U; "
+            "print(U.lib().ulysses_checked_build(), U.LIB_PATH.endswith('libulysses_checked.so'))")
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env={**os.environ, "ULYSSES_CHECKED": "1"},
+                         capture_output=True, text=True, check=True).stdout.split()
+    assert out == ["1", "True"]
