@@ -89,8 +89,8 @@ struct BwdLayout {
   static constexpr int kBar = kStat + NSTAGE * 2 * BMQ * 4;
   // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[2], ds_full[2], dsm_free,
   // dq_full[2], dq_empty, fin, drain, stg_full[NSTAGE], dk_done[NSTAGE],
-  // v_full, dp_free
-  static constexpr int kNumBar = 1 + 4 * NSTAGE + 7 + 3 + 2;
+  // v_full, dp_free, p_full[2]
+  static constexpr int kNumBar = 1 + 4 * NSTAGE + 7 + 3 + 4;
   static constexpr int kMisc = kBar + kNumBar * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -171,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dk_done = stg_full + NSTAGE;   // dK of a stage's tile done: its Q buffer is free
   uint64_t* v_full = dk_done + NSTAGE;     // V copied into TMEM
   uint64_t* dp_free = v_full + 1;          // every gradient warp has read the tile's dP^T
+  uint64_t* p_full = dp_free + 1;          // [2] P^T of the tile written to TMEM
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -197,6 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(v_full, kReadWarps);
     mbar_init(dp_free, kGradWarps);
+    mbar_init(&p_full[0], kGradWarps);
+    mbar_init(&p_full[1], kGradWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -307,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it + 1 < n_it && !issue_scores(it + 1)) { ok = false; break; }
       const int st = it % NSTAGE;
       const uint32_t b = (uint32_t)(it & 1);
-      if (!mbar_wait_warp(&ds_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&p_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       {
         // B = dO_it / Q_it as MN-major: 16 queries per step (2048 B), 64-feature
@@ -322,6 +325,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < BMQ / 16; ++kk)
           mma_ts_w(tbase + kColDV, tbase + kColS + b * BMQ + packed_col(kk), sdesc_add(dod, kk * 2048), id_g,
                    (it > 0 || kk > 0) ? 1u : 0u);
+        // dQ^T and dK read the dS^T tile in shared memory
+        if (!mbar_wait_warp(&ds_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
         // dQ^T = K^T dS^T into S buffer b: A = K (MN-major, 64-feature chunks
         // L::kChunkKV apart), B = dS^T ([key][query] rows of 128 B); 16 keys per step.
 #pragma unroll
@@ -507,6 +513,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         grad_cols(std::true_type{});
       // bf16 pairs: 16 columns per half, inside the half's own 32 columns
       tmem_st16(tbase + lane_off + kColS + b * BMQ + h * 32, pp);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[b]);
       // the dS^T tile in shared memory was last read by dQ^T_{it-1} and dK_{it-1}
       if (it >= 1 && !mbar_wait_warp(dsm_free, (it - 1) & 1, abort_flag)) { ok = false; break; }
       uint8_t* row = sDS + jr * 128;
@@ -517,8 +527,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(row + ((lc ^ (jr & 7)) << 4)) = w;
       }
       fence_async_smem();
-      tmem_st_wait();
-      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ds_full[b]);
     }
