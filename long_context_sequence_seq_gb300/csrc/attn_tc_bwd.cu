@@ -29,17 +29,23 @@
 // Four readout warps then read dQ_i^T out of TMEM (lane = feature d) and
 // write scale * dQ_i as [query][feature] fp32 rows into the tile's consumed
 // Q/dO stage buffers; a flusher warp adds them into dQ with TMA bulk
-// reduce-adds (cp.reduce.async.bulk) and then releases the stage.  Those fp32
-// reductions into L2 (32 KB per tile) bound this kernel at long S.
+// reduce-adds (cp.reduce.async.bulk) and then releases the stage.
 //
-// Warp roles (512 threads): 0 TMA producer, 1 TMEM owner and MMA issuer (whole
-// warp runs the issue code, one elected lane issues), 2 LSE/D_i loader, 3 dQ
-// flusher, 4-7 dQ^T readout (one per TMEM lane quarter), 8-15 gradient warps:
-// two per lane quarter, each taking 32 of the tile's 64 queries (thread = key
-// row).  Warpgroups 0-1 run on 112 registers per thread and give the rest to
-// the gradient warpgroups (144).  TMEM columns: dV [0,128), dK [128,256), two
-// S^T/P^T buffers [256,384) that also receive each tile's dQ^T, one dP^T
-// buffer [384,448) and V [448,512) (bf16, two features per column).
+// What bounds it: shared-memory bandwidth.  Per 64-query tile the tensor
+// core reads 176 KB of MMA operands from shared memory, TMA writes the 32 KB
+// Q/dO tile, the gradient warps write 16 KB of dS^T, and the dQ rows are
+// staged (32 KB written, 32 KB read by the bulk reductions): 272 KB, about
+// 2125 clk at 128 B/clk, against ~2500 clk per tile measured.
+//
+// Warp roles (512 threads): 0 TMA producer (lane 0) and LSE/D_i loader (all
+// lanes), 1 TMEM owner and score-MMA issuer, 2 gradient-MMA issuer (both
+// issue warp-wide, one elected lane issues), 3 dQ flusher, 4-7 dQ^T readout
+// (one per TMEM lane quarter), 8-15 gradient warps: two per lane quarter,
+// each taking 32 of the tile's 64 queries (thread = key row).  Warpgroups 0-1
+// run on 112 registers per thread and give the rest to the gradient
+// warpgroups (144).  TMEM columns: dV [0,128), dK [128,256), two S^T/P^T
+// buffers [256,384) that also receive each tile's dQ^T, one dP^T buffer
+// [384,448) and V [448,512) (bf16, two features per column).
 #include <type_traits>
 
 #include "internal.h"
@@ -90,7 +96,7 @@ struct BwdLayout {
   // kv_full, q_full[NSTAGE], q_empty[NSTAGE], s_full[2], ds_full[2], dsm_free,
   // dq_full[2], dq_empty, fin, drain, stg_full[NSTAGE], dk_done[NSTAGE],
   // v_full, dp_free, p_full[2]
-  static constexpr int kNumBar = 1 + 4 * NSTAGE + 7 + 3 + 4;
+  static constexpr int kNumBar = 1 + 4 * NSTAGE + 7 + 3 + 4 + 1 + 1;
   static constexpr int kMisc = kBar + kNumBar * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -126,19 +132,23 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   *reinterpret_cast<float4*>(dq + row * D + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
-// Pipeline (MMA issue order), it = iteration, b = it & 1:
-//   S^T_{it+1}, dP^T_{it+1}  -> s_full[b']         (needs Q/dO of it+1 and the
-//                                                   readout of dQ^T_{it-1}, which
-//                                                   lived in S buffer b')
-//   wait ds_full[b]  (gradient warps finished tile it)
-//   dV += P^T_it dO_it, dQ^T_it = K^T dS^T_it (into S buffer b) -> dq_full[b], dsm_free
-//   dK += dS^T_it Q_it                                             -> dk_done[stage]
-// so the tensor pipe runs tile it's gradient MMAs and tile it+1's score MMAs
-// while the gradient warps work on tile it+1.  dQ^T goes before dK so that its
-// readout (which frees S buffer b for the scores of it+2) overlaps dK; the
-// readout then waits for dk_done before it reuses the tile's Q buffer.  The
-// per-stage dk_done barrier cannot run two phases ahead of the readout: dK of
-// the stage's next tile needs the stage refilled, which needs this readout.
+// Pipeline, it = tile, b = it & 1.  Score issuer (warp 1), running ahead:
+//   S^T_it, dP^T_it -> s_full[b]   (needs Q/dO of it, the readout of dQ^T_{it-2}
+//                                    which lived in S buffer b, and every
+//                                    gradient warp done reading dP^T_{it-1})
+// Gradient issuer (warp 2):
+//   wait p_full[b]   dV += P^T_it dO_it
+//   wait ds_full[b]  dQ^T_it = K^T dS^T_it (into S buffer b) -> dq_full[b]
+//                    dK += dS^T_it Q_it                     -> dsm_free, dk_done[stage]
+// so the tensor pipe runs tile it's gradient MMAs and later tiles' score MMAs
+// while the gradient warps work.  dQ^T goes before dK so that its readout
+// (which frees S buffer b for the scores of it+2) overlaps dK; the readout
+// then waits for dk_done before it reuses the tile's Q buffer.  Barriers the
+// score issuer waits on are per buffer (dq_empty[b]) or cannot run a phase
+// ahead of it (dp_free, q_full need its own earlier MMAs), so parity waits
+// are unambiguous; the per-stage dk_done cannot run two phases ahead of the
+// readout: dK of the stage's next tile needs the stage refilled, which needs
+// this readout.
 __global__ void __launch_bounds__(kThreads, 1)
     tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -164,14 +174,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ds_full = s_full + 2;
   uint64_t* dsm_free = ds_full + 2;
   uint64_t* dq_full = dsm_free + 1;
-  uint64_t* dq_empty = dq_full + 2;
-  uint64_t* fin = dq_empty + 1;
+  uint64_t* dq_empty = dq_full + 2;       // [2] readout of the dQ^T in S buffer b done
+  uint64_t* fin = dq_empty + 2;
   uint64_t* drain = fin + 1;
   uint64_t* stg_full = drain + 1;     // dQ tile of a stage written to its Q/dO buffers
   uint64_t* dk_done = stg_full + NSTAGE;   // dK of a stage's tile done: its Q buffer is free
   uint64_t* v_full = dk_done + NSTAGE;     // V copied into TMEM
   uint64_t* dp_free = v_full + 1;          // every gradient warp has read the tile's dP^T
   uint64_t* p_full = dp_free + 1;          // [2] P^T of the tile written to TMEM
+  uint64_t* drain_s = p_full + 2;          // the score issuer's MMAs have all completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -192,7 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&ds_full[b], kGradWarps);
       mbar_init(&dq_full[b], 1);
     }
-    mbar_init(dq_empty, kReadWarps);
+    mbar_init(&dq_empty[0], kReadWarps);
+    mbar_init(&dq_empty[1], kReadWarps);
     mbar_init(dsm_free, 1);
     mbar_init(fin, 1);
     mbar_init(drain, 1);
@@ -200,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(dp_free, kGradWarps);
     mbar_init(&p_full[0], kGradWarps);
     mbar_init(&p_full[1], kGradWarps);
+    mbar_init(drain_s, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -227,35 +240,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_it = n_qb * G;   // iteration it -> q head g = it / n_qb, block qb = it % n_qb
 
   if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ TMA producer + LSE / D_i loader
+    // Lane 0 issues the TMA loads; every lane then loads two rows' LSE and
+    // D_i terms of the tile into the stage's stats (the second arrival on
+    // q_full).
     if (lane == 0) {
       mbar_expect_tx(kv_full, L::kTileKV);
       for (int c = 0; c < D / 64; ++c) {
         // head layout: (feature, row, head); sequence layout: (feature, head, row)
         tma_load_3d(sK + c * L::kChunkKV, &tmK, c * 64, seq ? kvh : (int)k0, seq ? (int)k0 : kvh, kv_full);
       }
-      for (int it = 0; it < n_it; ++it) {
-        const int st = it % NSTAGE;
-        const uint32_t round = it / NSTAGE;
-        if (!mbar_wait(&q_empty[st], (round & 1) ^ 1, abort_flag)) break;
-        const int n = kvh * G + it / n_qb;
-        const int q0 = (int)(q_lo + (int64_t)(it % n_qb) * BMQ);
-        mbar_expect_tx(&q_full[st], 2 * L::kTileQ);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(sQ + st * L::kTileQ + c * L::kChunkQ, &tmQ, c * 64, seq ? n : q0, seq ? q0 : n, &q_full[st]);
-          tma_load_3d(sDO + st * L::kTileQ + c * L::kChunkQ, &tmDO, c * 64, seq ? n : q0, seq ? q0 : n, &q_full[st]);
-        }
-      }
     }
     __syncwarp();
-  } else if (warp == 2) {
-    // ------------------------------------------------------------ LSE / D_i loader
     for (int it = 0; it < n_it; ++it) {
       const int st = it % NSTAGE;
       const uint32_t round = it / NSTAGE;
       if (!mbar_wait_warp(&q_empty[st], (round & 1) ^ 1, abort_flag)) break;
       const int n = kvh * G + it / n_qb;
       const int64_t q0 = q_lo + (int64_t)(it % n_qb) * BMQ;
+      if (lane == 0) {
+        mbar_expect_tx(&q_full[st], 2 * L::kTileQ);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(sQ + st * L::kTileQ + c * L::kChunkQ, &tmQ, c * 64, seq ? n : (int)q0, seq ? (int)q0 : n,
+                      &q_full[st]);
+          tma_load_3d(sDO + st * L::kTileQ + c * L::kChunkQ, &tmDO, c * 64, seq ? n : (int)q0, seq ? (int)q0 : n,
+                      &q_full[st]);
+        }
+      }
       float* stat = sStat + st * 2 * BMQ;
 #pragma unroll
       for (int r = lane; r < BMQ; r += 32) {
@@ -268,8 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&q_full[st]);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+    __syncwarp();
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues S^T and dP^T of every tile as soon as its stage, its S
+    // buffer and the dP^T buffer are free, running ahead of the gradient
+    // warps; warp 2 issues the gradient MMAs of each tile (dV once P^T is in
+    // TMEM, dQ^T and dK once dS^T is in shared memory).  MMAs of different
+    // warps are not ordered with respect to each other: every cross-warp
+    // dependency goes through an mbarrier (s_full, p_full, ds_full, dq_full
+    // -> readout -> dq_empty, dp_free, dsm_free).
     constexpr uint32_t id_s = idesc_bf16(BN, BMQ, false, false);    // S^T, dP^T
     constexpr uint32_t id_g = idesc_bf16(BN, D, false, true);       // dV, dK
     constexpr uint32_t id_q = idesc_bf16(D, BMQ, true, true);       // dQ^T
@@ -282,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t round = it / NSTAGE;
       if (!mbar_wait_warp(&q_full[st], round & 1, abort_flag)) return false;
       // S buffer of this parity held dQ^T_{it-2}: its readout must be done
-      if (it >= 2 && !mbar_wait_warp(dq_empty, (it - 2) & 1, abort_flag)) return false;
+      if (it >= 2 && !mbar_wait_warp(&dq_empty[it & 1], ((it - 2) >> 1) & 1, abort_flag)) return false;
       // the single dP^T buffer: every gradient warp has read dP^T_{it-1}
       if (it >= 1 && !mbar_wait_warp(dp_free, (it - 1) & 1, abort_flag)) return false;
       tc_fence_after();
@@ -304,49 +323,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       return true;
     };
-    bool ok = mbar_wait_warp(kv_full, 0, abort_flag) && mbar_wait_warp(v_full, 0, abort_flag);
-    if (ok && n_it > 0) ok = issue_scores(0);
-    for (int it = 0; ok && it < n_it; ++it) {
-      if (it + 1 < n_it && !issue_scores(it + 1)) { ok = false; break; }
-      const int st = it % NSTAGE;
-      const uint32_t b = (uint32_t)(it & 1);
-      if (!mbar_wait_warp(&p_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
-      tc_fence_after();
-      {
-        // B = dO_it / Q_it as MN-major: 16 queries per step (2048 B), 64-feature
-        // chunks L::kChunkQ apart.
-        const uint64_t dod = sdesc_sw128(smem_u32(sDO + st * L::kTileQ), L::kChunkQ, 1024);
-        const uint64_t qd = sdesc_sw128(smem_u32(sQ + st * L::kTileQ), L::kChunkQ, 1024);
-        const uint64_t dsd = sdesc_sw128(smem_u32(sDS), 8192, 1024);
-        // dV first (it reads P^T from S buffer b), then dQ^T into S buffer b, then
-        // dK: the dQ^T readout overlaps dK, so the next scores into buffer b
-        // wait less.  dK reads the dS^T tile in shared memory (K-major A).
-#pragma unroll
-        for (int kk = 0; kk < BMQ / 16; ++kk)
-          mma_ts_w(tbase + kColDV, tbase + kColS + b * BMQ + packed_col(kk), sdesc_add(dod, kk * 2048), id_g,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-        // dQ^T and dK read the dS^T tile in shared memory
-        if (!mbar_wait_warp(&ds_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
+    if (warp == 1) {
+      bool ok = mbar_wait_warp(kv_full, 0, abort_flag) && mbar_wait_warp(v_full, 0, abort_flag);
+      for (int it = 0; ok && it < n_it; ++it) ok = issue_scores(it);
+      mma_commit_w(drain_s);
+      mbar_wait(drain_s, 0, nullptr);
+    } else {
+      bool ok = mbar_wait_warp(kv_full, 0, abort_flag);
+      for (int it = 0; ok && it < n_it; ++it) {
+        const int st = it % NSTAGE;
+        const uint32_t b = (uint32_t)(it & 1);
+        if (!mbar_wait_warp(&p_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        // dQ^T = K^T dS^T into S buffer b: A = K (MN-major, 64-feature chunks
-        // L::kChunkKV apart), B = dS^T ([key][query] rows of 128 B); 16 keys per step.
-#pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ss_w(tbase + kColS + b * BMQ, sdesc_add(kd_mn, kk * 2048), sdesc_add(dsd, kk * 2048), id_q,
-                   kk > 0 ? 1u : 0u);
-        mma_commit_w(&dq_full[b]);
-#pragma unroll
-        for (int kk = 0; kk < BMQ / 16; ++kk)
-          mma_ss_w(tbase + kColDK, sdesc_add(dsd_k, kk * 32), sdesc_add(qd, kk * 2048), id_g,
-                   (it > 0 || kk > 0) ? 1u : 0u);
-        mma_commit_w(dsm_free);
-        mma_commit_w(&dk_done[st]);
+        {
+          // B = dO_it / Q_it as MN-major: 16 queries per step (2048 B), 64-feature
+          // chunks L::kChunkQ apart.
+          const uint64_t dod = sdesc_sw128(smem_u32(sDO + st * L::kTileQ), L::kChunkQ, 1024);
+          const uint64_t qd = sdesc_sw128(smem_u32(sQ + st * L::kTileQ), L::kChunkQ, 1024);
+          const uint64_t dsd = sdesc_sw128(smem_u32(sDS), 8192, 1024);
+          // dV first (it reads P^T from S buffer b), then dQ^T into S buffer b, then
+          // dK: the dQ^T readout overlaps dK, so the next scores into buffer b
+          // wait less.  dK reads the dS^T tile in shared memory (K-major A).
+  #pragma unroll
+          for (int kk = 0; kk < BMQ / 16; ++kk)
+            mma_ts_w(tbase + kColDV, tbase + kColS + b * BMQ + packed_col(kk), sdesc_add(dod, kk * 2048), id_g,
+                     (it > 0 || kk > 0) ? 1u : 0u);
+          // dQ^T and dK read the dS^T tile in shared memory
+          if (!mbar_wait_warp(&ds_full[b], (it >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          // dQ^T = K^T dS^T into S buffer b: A = K (MN-major, 64-feature chunks
+          // L::kChunkKV apart), B = dS^T ([key][query] rows of 128 B); 16 keys per step.
+  #pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ss_w(tbase + kColS + b * BMQ, sdesc_add(kd_mn, kk * 2048), sdesc_add(dsd, kk * 2048), id_q,
+                     kk > 0 ? 1u : 0u);
+          mma_commit_w(&dq_full[b]);
+  #pragma unroll
+          for (int kk = 0; kk < BMQ / 16; ++kk)
+            mma_ss_w(tbase + kColDK, sdesc_add(dsd_k, kk * 32), sdesc_add(qd, kk * 2048), id_g,
+                     (it > 0 || kk > 0) ? 1u : 0u);
+          mma_commit_w(dsm_free);
+          mma_commit_w(&dk_done[st]);
+        }
+        __syncwarp();
       }
-      __syncwarp();
+      mma_commit_w(fin);
+      mma_commit_w(drain);
+      mbar_wait(drain, 0, nullptr);
     }
-    mma_commit_w(fin);
-    mma_commit_w(drain);
-    mbar_wait(drain, 0, nullptr);
   } else if (warp == 3) {
     // ------------------------------------------------------------ dQ flusher
     // Tile x's dQ rows sit in its (consumed) Q buffer (rows 0-31) and dO
@@ -431,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence(r1);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(dq_empty);
+      if (lane == 0) mbar_arrive(&dq_empty[bx]);
       float* c0 = reinterpret_cast<float*>(sQ + sx * L::kTileQ) + d;
       float* c1 = reinterpret_cast<float*>(sDO + sx * L::kTileQ) + d;
       // queries 32-63 into the dO buffer (dV, which read it, is done) ...
