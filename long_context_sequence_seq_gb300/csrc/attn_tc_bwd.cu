@@ -31,11 +31,12 @@
 // Q/dO stage buffers; a flusher warp adds them into dQ with TMA bulk
 // reduce-adds (cp.reduce.async.bulk) and then releases the stage.
 //
-// What bounds it: shared-memory bandwidth.  Per 64-query tile the tensor
-// core reads 176 KB of MMA operands from shared memory, TMA writes the 32 KB
-// Q/dO tile, the gradient warps write 16 KB of dS^T, and the dQ rows are
-// staged (32 KB written, 32 KB read by the bulk reductions): 272 KB, about
-// 2125 clk at 128 B/clk, against ~2500 clk per tile measured.
+// What bounds it: neither the tensor pipe nor shared memory saturates (at a
+// 16K stage: tensor pipe 51% of active cycles, shared-memory banks 27% read /
+// 11% write).  The MMAs of one tile take ~1540 clk at full rate against ~2500
+// clk per tile, and the period follows the gradient warps' per-tile work plus
+// the chain dS^T -> dQ^T -> readout -> next scores that the two S buffers
+// only partly hide.
 //
 // Warp roles (512 threads): 0 TMA producer (lane 0) and LSE/D_i loader (all
 // lanes), 1 TMEM owner and score-MMA issuer, 2 gradient-MMA issuer (both
@@ -132,6 +133,92 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const __nv_bfloat16* __res
   *reinterpret_cast<float4*>(dq + row * D + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// Work of a key block: the 64-query tiles that see its keys (the same range
+// the kernel walks).
+__device__ __forceinline__ int key_block_work(int kb, const int32_t* __restrict__ cu, int nd, int64_t S,
+                                              int causal) {
+  const int64_t k0 = (int64_t)kb * BN;
+  const int64_t last_key = (k0 + BN < S ? k0 + BN : S) - 1;
+  int64_t q_lo, q_hi, tmp;
+  query_range(cu, nd, S, causal, k0, q_lo, tmp);
+  query_range(cu, nd, S, causal, last_key, tmp, q_hi);
+  q_lo = (q_lo / BMQ) * BMQ;
+  return q_hi > q_lo ? (int)((q_hi - q_lo + BMQ - 1) / BMQ) : 0;
+}
+
+// Block-wide sum of a per-thread count in [0, 16) through __syncthreads_count
+// on its bits (every thread of the CTA must call it).
+__device__ __forceinline__ int block_count16(int c) {
+  return __syncthreads_count(c & 1) + 2 * __syncthreads_count(c & 2) + 4 * __syncthreads_count(c & 4) +
+         8 * __syncthreads_count(c & 8);
+}
+
+// With packed documents the work of a key block depends on its document, so
+// key blocks in index order leave a heavy block of a late document to start
+// near the end of the grid.  Rank r of the grid gets instead the r-th key
+// block in decreasing work (ties: lower block first), the longest-processing-
+// time order a list scheduler such as the block scheduler handles best.  Every
+// CTA selects its own block: it evaluates the work of all nkb blocks (kLptPer
+// per thread), finds by bisection the work value t of rank r (the least t
+// with fewer than r + 1 blocks above it), then the block among those of work
+// t.  All threads of the CTA call it; `scratch` holds 33 words.
+constexpr int kLptPer = 8;
+constexpr int kLptMaxBlocks = kLptPer * kThreads;
+__device__ int lpt_key_block(int r, int nkb, const int32_t* __restrict__ cu, int nd, int64_t S, int causal,
+                             int* scratch) {
+  int wk[kLptPer];
+  int wmax = 0;
+#pragma unroll
+  for (int i = 0; i < kLptPer; ++i) {
+    const int kb = (int)threadIdx.x + i * kThreads;
+    wk[i] = kb < nkb ? key_block_work(kb, cu, nd, S, causal) : -1;
+    wmax = wk[i] > wmax ? wk[i] : wmax;
+  }
+  auto count_above = [&](int t) {
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < kLptPer; ++i) c += wk[i] > t ? 1 : 0;
+    return block_count16(c);
+  };
+  // the largest work in the CTA: bisection bound (every thread takes part)
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int o = 16; o > 0; o >>= 1) wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+  if (lane == 0) scratch[warp] = wmax;
+  __syncthreads();
+  int hi = 0;
+  for (int w = 0; w < kThreads / 32; ++w) hi = max(hi, scratch[w]);
+  __syncthreads();
+  int lo = 0;   // count_above(hi) == 0 <= r
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (count_above(mid) <= r) hi = mid; else lo = mid + 1;
+  }
+  int idx = r - count_above(lo);   // rank among the blocks of work lo, in index order
+  int result = -1;
+#pragma unroll
+  for (int i = 0; i < kLptPer; ++i) {
+    if (result >= 0) continue;   // uniform over the CTA
+    const bool m = wk[i] == lo;
+    const int ci = __syncthreads_count(m);
+    if (idx < ci) {
+      // exclusive prefix of m over thread index (block index order in chunk i)
+      const unsigned bal = __ballot_sync(0xffffffffu, m);
+      if (lane == 0) scratch[warp] = __popc(bal);
+      __syncthreads();
+      int before = __popc(bal & ((1u << lane) - 1u));
+      for (int w = 0; w < warp; ++w) before += scratch[w];
+      if (m && before == idx) scratch[32] = (int)threadIdx.x + i * kThreads;
+      __syncthreads();
+      result = scratch[32];
+    } else {
+      idx -= ci;
+    }
+  }
+  fence_async_smem();   // the scratch words are overwritten by TMA later
+  __syncthreads();
+  return result < 0 ? 0 : result;
+}
+
 // Pipeline, it = tile, b = it & 1.  Score issuer (warp 1), running ahead:
 //   S^T_it, dP^T_it -> s_full[b]   (needs Q/dO of it, the readout of dQ^T_{it-2}
 //                                    which lived in S buffer b, and every
@@ -188,7 +275,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int kvh = blockIdx.x;                          // kv head in the buffer
-  const int64_t k0 = (int64_t)blockIdx.y * BN;         // first key of the block
+  // key block: in index order (already decreasing work without documents),
+  // or in decreasing work for packed documents; the Q stage area is free
+  // scratch until the first TMA load
+  const int kb = (cu != nullptr && gridDim.y <= kLptMaxBlocks)
+                     ? lpt_key_block((int)blockIdx.y, (int)gridDim.y, cu, nd, S, causal,
+                                     reinterpret_cast<int*>(sQ))
+                     : (int)blockIdx.y;
+  const int64_t k0 = (int64_t)kb * BN;                 // first key of the block
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);

@@ -56,6 +56,9 @@ SMALL = [
     (260, 4, 2, 64, 2, 2, "bf16", None, True),
     (256, 8, 8, 64, 2, 4, "fp32", None, True),
     (130, 4, 2, 128, 2, 2, "fp32", [60, 70], True),
+    # many key blocks of unequal work: the backward's decreasing-work block order
+    (3000, 4, 2, 128, 1, 4, "bf16", [700, 5, 123, 1000, 128, 256, 300, 488], True),
+    (2100, 4, 2, 128, 1, 4, "bf16", [128, 512, 640, 64, 756], False),
 ]
 
 
