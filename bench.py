@@ -43,7 +43,7 @@ NOMINAL_HBM_GBS = 7900.0
 # DRAM bytes per launch of the dominant kernel from an ncu capture of this
 # workload, valid only for the kernel source it was taken on (sha256 prefix);
 # any other source reports null.
-TRAFFIC = {"qwen3_4b_64k": ("attn_tc_bwd.cu", "3154fc4b7be8c7b5", 3539614656)}
+TRAFFIC = {"qwen3_4b_64k": ("attn_tc_bwd.cu", "b5a16aedd5cff6b1", 3267981760)}
 
 
 def measured_traffic(workload):

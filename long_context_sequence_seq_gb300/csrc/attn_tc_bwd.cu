@@ -33,10 +33,14 @@
 //
 // What bounds it: neither the tensor pipe nor shared memory saturates (at a
 // 16K stage: tensor pipe 51% of active cycles, shared-memory banks 27% read /
-// 11% write).  The MMAs of one tile take ~1540 clk at full rate against ~2500
-// clk per tile, and the period follows the gradient warps' per-tile work plus
-// the chain dS^T -> dQ^T -> readout -> next scores that the two S buffers
-// only partly hide.
+// 11% write); the MMAs of a tile take ~1540 clk at full rate against ~2540
+// clk per tile.  An event trace of one CTA at S = 64K shows the period equal
+// to a Q/dO stage's lifetime over the five stages: a stage is held from its
+// TMA load (~3000 clk to arrive: the same TMA unit carries the dQ reductions)
+// through the tile's MMAs and gradient work to the flusher's reductions of
+// the dQ rows staged in it (~2100 clk for 32 KB).  Timing-only variants that
+// skip work: no dQ reductions +7%, half of them +5%, no Q/dO loads +5%, no
+// P/dS arithmetic +5%.
 //
 // Warp roles (512 threads): 0 TMA producer (lane 0) and LSE/D_i loader (all
 // lanes), 1 TMEM owner and score-MMA issuer, 2 gradient-MMA issuer (both
