@@ -22,6 +22,14 @@
 // S is triple-buffered in TMEM, so QK_{j+1} and QK_{j+2} can run on the tensor
 // pipe while the softmax works on tile j, and PV_j overlaps softmax j+1.
 //
+// The CTAs of the G q heads of one kv head (same query tile) form a cluster
+// of up to four: they read the same K/V tiles, so each CTA loads 1/CL of a
+// tile's rows and multicasts them into every CTA's slot, and a slot is
+// refilled once every CTA's QK_j (K) or PV_j (V) has completed (commits
+// multicast to all the cluster's empty barriers).  This cuts the K/V reads
+// from L2 by CL and keeps the cluster's CTAs on the same keys, which matters
+// once K/V outgrow L2 (million-token stages).
+//
 // TMEM columns (512 allocated): S/P buffers [0,128), [128,256), [256,384);
 // O accumulator [384, 384+D).
 // Shared memory: Q tile (D/64 swizzle-128B chunks of 128 rows) + the K ring
@@ -64,14 +72,15 @@ struct FwdLayout {
   static constexpr int kQ = 0;
   static constexpr int kKV = kQ + kTileQ;
   static constexpr int kBar = kKV + NSLOT * kTileKV;
-  // q_full, k_full/v_full[NRING], k_empty/v_empty[NRING], s_full[NSBUF], p_full[NSBUF], drain[2]
-  static constexpr int kNumBar = 1 + 4 * NRING + 2 * NSBUF + 2;
+  // q_full, k_full/v_full[NRING], k_empty/v_empty[NRING], s_full[NSBUF], p_full[NSBUF], drain[2],
+  // v_free[NRING]
+  static constexpr int kNumBar = 1 + 4 * NRING + 2 * NSBUF + 2 + NRING;
   static constexpr int kMisc = kBar + kNumBar * 8;
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;        // slack for 1024-byte alignment
 };
 
-template <int D>
+template <int D, int CL>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ out,
@@ -94,6 +103,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s_full = v_empty + NRING;
   uint64_t* p_full = s_full + NSBUF;
   uint64_t* drain = p_full + NSBUF;
+  // with a cluster: v_free[j % NRING] completes when PV_j has run in every CTA
+  // of the cluster (the V slot may be refilled); k_empty counts every CTA's QK_j
+  uint64_t* v_free = drain + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -105,7 +117,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int s = 0; s < 4 * NRING; ++s) mbar_init(&k_full[s], 1);   // k/v full, k/v empty
+    for (int s = 0; s < 2 * NRING; ++s) mbar_init(&k_full[s], 1);          // k/v full
+    for (int s = 0; s < NRING; ++s) mbar_init(&k_empty[s], CL);             // every CTA's QK_j
+    for (int s = 0; s < NRING; ++s) mbar_init(&v_empty[s], 1);              // this CTA's PV_j
+    for (int s = 0; s < NRING; ++s) mbar_init(&v_free[s], CL);              // every CTA's PV_j
     for (int b = 0; b < NSBUF; ++b) { mbar_init(&s_full[b], 1); mbar_init(&p_full[b], 4); }
     mbar_init(&drain[0], 1);
     mbar_init(&drain[1], 1);
@@ -123,8 +138,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  // the cluster's barriers are initialised before any CTA loads into or
+  // arrives on another's
+  if constexpr (CL > 1) cluster_sync();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  const uint32_t crank = CL > 1 ? cluster_ctarank() : 0u;
+  constexpr uint16_t kMask = (uint16_t)((1u << CL) - 1u);
 
   // Key tiles of this CTA: [kv_lo, kv_hi) in steps of BN.
   const int64_t last_row = (q0 + BM < S ? q0 + BM : S) - 1;
@@ -148,14 +168,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int j = kv ? t - 1 : t;
           if (j < 0 || j >= n_kv) continue;
           const int r = j % NRING;
-          uint64_t* empty = kv ? &v_empty[r] : &k_empty[r];
+          uint64_t* empty = kv ? (CL > 1 ? &v_free[r] : &v_empty[r]) : &k_empty[r];
           uint64_t* full = kv ? &v_full[r] : &k_full[r];
           if (!mbar_wait(empty, ((uint32_t)(j / NRING) & 1u) ^ 1u, abort_flag)) { go = false; break; }
           mbar_expect_tx(full, L::kTileKV);
           const int k0 = (int)(kv_lo + (int64_t)j * BN);
           uint8_t* dst = sKV + (kv * NRING + r) * L::kTileKV;
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(dst + c * L::kChunkKV, kv ? &tmV : &tmK, c * 64, seq ? kvh : k0, seq ? k0 : kvh, full);
+          if constexpr (CL > 1) {
+            // this CTA's share of the tile: rows [crank BN/CL, (crank+1) BN/CL),
+            // multicast into the same slot of every CTA of the cluster
+            const int kr = k0 + (int)crank * (BN / CL);
+            uint8_t* part = dst + crank * (BN / CL) * 128;
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d_mc(part + c * L::kChunkKV, kv ? &tmV : &tmK, c * 64, seq ? kvh : kr, seq ? kr : kvh, full,
+                             kMask);
+          } else {
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d(dst + c * L::kChunkKV, kv ? &tmV : &tmK, c * 64, seq ? kvh : k0, seq ? k0 : kvh, full);
+          }
         }
     }
     __syncwarp();
@@ -194,7 +224,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss_w(d_tmem, sdesc_add(qdesc, off), sdesc_add(kdesc, offk), idesc_qk, kk > 0 ? 1u : 0u);
         }
         mma_commit_w(&s_full[j % NSBUF]);
-        mma_commit_w(&k_empty[slot]);
+        if constexpr (CL > 1) mma_commit_mc_w(&k_empty[slot], kMask);
+        else mma_commit_w(&k_empty[slot]);
       }
       // drain: nothing of ours may still be in flight at teardown
       mma_commit_w(&drain[0]);
@@ -215,6 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ts_w(tbase + kColO, p_tmem + kk * 8, sdesc_add(vdesc, kk * 2048), idesc_pv,
                    (j > 0 || kk > 0) ? 1u : 0u);
         mma_commit_w(&v_empty[r]);
+        if constexpr (CL > 1) mma_commit_mc_w(&v_free[r], kMask);
       }
       mma_commit_w(&drain[1]);
       mbar_wait(&drain[1], 0, nullptr);
@@ -350,32 +382,60 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
+  // no CTA retires while another of its cluster may still address it
+  if constexpr (CL > 1) cluster_sync();
 }
 
-template <int D>
-int launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
+// Cluster size: the CTAs of the G q heads of one kv head (same query tile)
+// share each K/V tile, every CTA loading 1/CL of its rows and multicasting
+// them to the others; 4 at most.
+inline int fwd_cluster(int G) { return G % 4 == 0 ? 4 : (G % 2 == 0 ? 2 : 1); }
+
+template <int D, int CL>
+int launch_fwd_dc(const AttnArgs& a, cudaStream_t st) {
   CUtensorMap tq, tk, tv;
   const int n_kv = a.n_q / a.G;
   int rc;
   if (a.seq) {
     if ((rc = make_tmap_bf16_seq(&tq, a.q, a.S, a.n_q, a.hq_tot, D, BM))) return rc;
-    if ((rc = make_tmap_bf16_seq(&tk, a.k, a.S, n_kv, a.hkv_tot, D, BN))) return rc;
-    if ((rc = make_tmap_bf16_seq(&tv, a.v, a.S, n_kv, a.hkv_tot, D, BN))) return rc;
+    if ((rc = make_tmap_bf16_seq(&tk, a.k, a.S, n_kv, a.hkv_tot, D, BN / CL))) return rc;
+    if ((rc = make_tmap_bf16_seq(&tv, a.v, a.S, n_kv, a.hkv_tot, D, BN / CL))) return rc;
   } else {
     if ((rc = make_tmap_bf16_3d(&tq, a.q, a.S, a.n_q, D, BM))) return rc;
-    if ((rc = make_tmap_bf16_3d(&tk, a.k, a.S, n_kv, D, BN))) return rc;
-    if ((rc = make_tmap_bf16_3d(&tv, a.v, a.S, n_kv, D, BN))) return rc;
+    if ((rc = make_tmap_bf16_3d(&tk, a.k, a.S, n_kv, D, BN / CL))) return rc;
+    if ((rc = make_tmap_bf16_3d(&tv, a.v, a.S, n_kv, D, BN / CL))) return rc;
   }
   const int smem = FwdLayout<D>::kAlloc;
-  static PerDeviceOnce<> smem_once;   // one per head dim (template instance)
-  if ((rc = opt_in_smem(smem_once, (const void*)tc_fwd_kernel<D>, smem, "tc_fwd"))) return rc;
+  static PerDeviceOnce<> smem_once;   // one per (head dim, cluster size) instance
+  if ((rc = opt_in_smem(smem_once, (const void*)tc_fwd_kernel<D, CL>, smem, "tc_fwd"))) return rc;
   const int64_t n_qt = (a.S + BM - 1) / BM;
-  dim3 grid((unsigned)a.n_q, (unsigned)n_qt);
-  tc_fwd_kernel<D><<<grid, kThreads, smem, st>>>(tq, tk, tv, (__nv_bfloat16*)a.o_out, a.lse, a.S,
-                                                 a.nq, a.G, a.lse_bstride, a.cu, a.nd, a.causal,
-                                                 a.scale * kLog2e, a.seq, a.hq_tot);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.n_q, (unsigned)n_qt);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, tc_fwd_kernel<D, CL>, tq, tk, tv, (__nv_bfloat16*)a.o_out, a.lse, a.S, a.nq, a.G,
+                     a.lse_bstride, a.cu, a.nd, a.causal, a.scale * kLog2e, a.seq, a.hq_tot);
   count_launch();
   return check_launch("tc_fwd");
+}
+
+template <int D>
+int launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
+  // the grid's x (q heads of the buffer) holds whole kv groups, so a cluster
+  // along x never spans two kv heads
+  switch (fwd_cluster(a.G)) {
+    case 4: return launch_fwd_dc<D, 4>(a, st);
+    case 2: return launch_fwd_dc<D, 2>(a, st);
+    default: return launch_fwd_dc<D, 1>(a, st);
+  }
 }
 
 }  // namespace
