@@ -22,13 +22,14 @@
 // S is triple-buffered in TMEM, so QK_{j+1} and QK_{j+2} can run on the tensor
 // pipe while the softmax works on tile j, and PV_j overlaps softmax j+1.
 //
-// The CTAs of the G q heads of one kv head (same query tile) form a cluster
-// of up to four: they read the same K/V tiles, so each CTA loads 1/CL of a
-// tile's rows and multicasts them into every CTA's slot, and a slot is
-// refilled once every CTA's QK_j (K) or PV_j (V) has completed (commits
-// multicast to all the cluster's empty barriers).  This cuts the K/V reads
-// from L2 by CL and keeps the cluster's CTAs on the same keys, which matters
-// once K/V outgrow L2 (million-token stages).
+// Two CTAs of q heads that share a kv head (same query tile) form a cluster:
+// they read the same K/V tiles, so each CTA loads half of a tile's rows and
+// multicasts them into both CTAs' slot, and a slot is refilled once both
+// CTAs' QK_j (K) or PV_j (V) have completed (commits multicast to both empty
+// barriers).  This halves the K/V reads from L2 and keeps the pair on the
+// same keys, which matters once K/V outgrow L2 (million-token stages).
+// Clusters of four would quarter them, but only 36 such clusters fit on the
+// GPU at once (144 of 152 SMs), which costs more than it saves.
 //
 // TMEM columns (512 allocated): S/P buffers [0,128), [128,256), [256,384);
 // O accumulator [384, 384+D).
@@ -386,10 +387,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (CL > 1) cluster_sync();
 }
 
-// Cluster size: the CTAs of the G q heads of one kv head (same query tile)
-// share each K/V tile, every CTA loading 1/CL of its rows and multicasting
-// them to the others; 4 at most.
-inline int fwd_cluster(int G) { return G % 4 == 0 ? 4 : (G % 2 == 0 ? 2 : 1); }
+// Cluster size: two CTAs of q heads that share a kv head (same query tile)
+// share each K/V tile, each loading half of its rows and multicasting them to
+// the other; one CTA without GQA.
+inline int fwd_cluster(int G) { return G % 2 == 0 ? 2 : 1; }
 
 template <int D, int CL>
 int launch_fwd_dc(const AttnArgs& a, cudaStream_t st) {
@@ -431,11 +432,7 @@ template <int D>
 int launch_fwd_d(const AttnArgs& a, cudaStream_t st) {
   // the grid's x (q heads of the buffer) holds whole kv groups, so a cluster
   // along x never spans two kv heads
-  switch (fwd_cluster(a.G)) {
-    case 4: return launch_fwd_dc<D, 4>(a, st);
-    case 2: return launch_fwd_dc<D, 2>(a, st);
-    default: return launch_fwd_dc<D, 1>(a, st);
-  }
+  return fwd_cluster(a.G) == 2 ? launch_fwd_dc<D, 2>(a, st) : launch_fwd_dc<D, 1>(a, st);
 }
 
 }  // namespace
