@@ -491,11 +491,13 @@ def fused_measure(w, dev, cu_np, steps, warmup):
             "note": "all-to-alls folded into the attention kernels' addressing"}
 
 
-def cpu_baseline(w, cu_np, budget_s=12.0):
+def cpu_baseline(w, cu_np, min_sample_s=7.5):
     """The fp64 oracle as it stands on the host cores, on a bounded sample:
     forward + backward of one (q head, kv head) pair over a causal prefix of
-    the sequence.  Reported as the full-workload tokens/s it implies
-    (pairs per second of the oracle, scaled to all heads and pairs)."""
+    the sequence, the prefix doubled until one pass takes more than
+    min_sample_s (so the timed pass takes ~8-30 s).  Reported as the
+    full-workload tokens/s it implies (pairs per second of the oracle, scaled
+    to all heads and pairs)."""
     import oracle
     cores = len(os.sched_getaffinity(0))
     L = 2048
@@ -509,7 +511,7 @@ def cpu_baseline(w, cu_np, budget_s=12.0):
         oracle.attn_fwd(q, k, v)
         oracle.attn_bwd(q, k, v, do)
         dt = time.perf_counter() - t0
-        if dt > budget_s / 4 or L >= w.S:
+        if dt > min_sample_s or L >= w.S:
             break
         L = min(w.S, L * 2)
     pairs_s = (L * (L + 1) / 2) / dt
@@ -634,10 +636,10 @@ def reference_arm(args):
     w = workload_from_args(args)
     cu_np = inputs.workload_cu_seqlens(w)
     for _ in range(args.warmup):
-        cpu_baseline(w, cu_np, budget_s=2.0)
+        cpu_baseline(w, cu_np, min_sample_s=0.5)
     vals, secs = [], []
     for _ in range(args.steps):
-        r = cpu_baseline(w, cu_np, budget_s=2.0)
+        r = cpu_baseline(w, cu_np, min_sample_s=0.5)
         vals.append(r["value"])
         secs.append(r["sample_seconds"])
     v = statistics.median(vals)

@@ -91,6 +91,34 @@ def test_attention_small(S, Hq, Hkv, D, P, C, dtype, docs, causal):
         assert float((lq - dq).abs().max()) <= 1e-5 * max(1.0, float(dq.abs().max()))
 
 
+@pytest.mark.parametrize("S,Hq,Hkv,P,C,causal", [
+    (300, 8, 2, 2, 4, True),     # G = 4: pair clusters in the forward, both batch entries
+    (257, 8, 1, 1, 8, True),     # G = 8, ragged S
+    (200, 4, 4, 2, 2, False),    # G = 1 (no cluster), bidirectional
+])
+def test_layer_batch_of_two(S, Hq, Hkv, P, C, causal):
+    """B = 2 through the layer drivers: the stages' buffers hold both batch
+    entries' heads, so kv-head mapping, LSE strides and clusters must not mix
+    them."""
+    D = 128
+    q, k, v, do = seq_inputs(S, Hq, Hkv, D, "bf16", B=2)
+    o, lse = U.layer_fwd(q, k, v, P, C, causal=causal)
+    dq, dk, dv = U.layer_bwd(q, k, v, o, do, lse, P, C, causal=causal)
+    U.check()
+    Q, K, V, DO = f64(q), f64(k), f64(v), f64(do)
+    ro, rl = oracle.ulysses_attention(Q, K, V, P, C, None, causal)
+    rq, rk, rv = oracle.ulysses_attention_bwd(Q, K, V, DO, P, C, None, causal)
+    assert max_err(f64(o), ro) <= TOL["bf16"]
+    assert max_err(f64(lse), rl) <= LSE_TOL["bf16"]
+    assert max_err(f64(dq), rq) <= TOL["bf16"]
+    assert max_err(f64(dk), rk) <= TOL["bf16"]
+    assert max_err(f64(dv), rv) <= TOL["bf16"]
+    # the two batch entries are independent problems
+    o1, l1 = U.layer_fwd(q[1:].contiguous(), k[1:].contiguous(), v[1:].contiguous(), P, C, causal=causal)
+    U.check()
+    assert torch.equal(o1, o[1:]) and torch.equal(l1, lse[1:])
+
+
 def test_tiny_mha_fp32_workload_all_chunks():
     """S=256, 8 heads, D=64, P=2, fp32: full oracle, head_chunk in {1, 2, 4}."""
     w = inputs.WORKLOADS["tiny_mha_fp32"]
