@@ -309,26 +309,27 @@ def e2e_measure(w, dev, cu_np, steps, warmup):
     cu = None if cu_np is None else torch.from_numpy(cu_np).to(dev)
     o = torch.empty(hq.shape, dtype=dt, device=dev)
     lse = torch.empty((w.B, w.H_q, w.S), dtype=torch.float32, device=dev)
-    dq = torch.empty(hq.shape, dtype=torch.float32, device=dev)
-    dk = torch.empty(hk.shape, dtype=torch.float32, device=dev)
-    dv = torch.empty(hv.shape, dtype=torch.float32, device=dev)
+    # two sets of device gradients: step i's download runs under step i+1
+    grads = [[torch.empty(t.shape, dtype=torch.float32, device=dev) for t in (hq, hk, hv)] for _ in range(2)]
     ho = torch.empty(o.shape, dtype=dt).pin_memory()
-    hdq = torch.empty(dq.shape, dtype=torch.float32).pin_memory()
-    hdk = torch.empty(dk.shape, dtype=torch.float32).pin_memory()
-    hdv = torch.empty(dv.shape, dtype=torch.float32).pin_memory()
+    hdq = torch.empty(hq.shape, dtype=torch.float32).pin_memory()
+    hdk = torch.empty(hk.shape, dtype=torch.float32).pin_memory()
+    hdv = torch.empty(hv.shape, dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (ho, hdq, hdk, hdv))
 
     # Copies run on two side streams, one per direction (separate copy
     # engines): step i's inputs are uploaded into buffer set i % 2 while step
-    # i-1 computes from the other set; O is downloaded under the backward and
-    # dQ/dK/dV under the next step's forward.  Events order every reuse of a
-    # buffer, so every step still moves all of its inputs and results.
+    # i-1 computes from the other set; O is downloaded under the backward, and
+    # dQ/dK/dV (gradient set i % 2) under the whole next step.  Events order
+    # every reuse of a buffer, so every step still moves all of its inputs and
+    # results.
     main = torch.cuda.current_stream(dev)
     up, down = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]        # set j uploaded
     ev_used = [torch.cuda.Event() for _ in range(2)]      # set j no longer read
-    ev = {name: torch.cuda.Event() for name in ("fwd", "o_out", "bwd", "g_out")}
+    ev = {name: torch.cuda.Event() for name in ("fwd", "o_out", "bwd")}
+    ev_g_out = [torch.cuda.Event() for _ in range(2)]     # gradient set j is on the host
     state = {"i": 0}
 
     def upload(i):
@@ -355,8 +356,9 @@ def e2e_measure(w, dev, cu_np, steps, warmup):
             ev["o_out"].record(down)
         if not last:
             upload(i + 1)                         # the next step's inputs, under this step
-        if i > 0:
-            main.wait_event(ev["g_out"])          # the previous gradients are on the host
+        dq, dk, dv = grads[j]
+        if i >= 2:
+            main.wait_event(ev_g_out[j])          # this set's gradients (step i-2) are on the host
         U.layer_bwd(q, k, v, o, do, lse, w.P, w.head_chunk, cu, w.causal, workspace=ws,
                     dq=dq, dk=dk, dv=dv)
         ev_used[j].record(main)
@@ -365,7 +367,7 @@ def e2e_measure(w, dev, cu_np, steps, warmup):
             down.wait_event(ev["bwd"])
             for h_, d_ in ((hdq, dq), (hdk, dk), (hdv, dv)):
                 h_.copy_(d_, non_blocking=True)
-            ev["g_out"].record(down)
+            ev_g_out[j].record(down)
         state["i"] = i + 1
 
     def run(n):
@@ -373,7 +375,8 @@ def e2e_measure(w, dev, cu_np, steps, warmup):
         upload(0)
         for s_ in range(n):
             step(s_ == n - 1)
-        main.wait_event(ev["g_out"])              # the last step's results are on the host
+        for e_ in ev_g_out:                       # every step's results are on the host
+            main.wait_event(e_)
 
     run(warmup)
     torch.cuda.synchronize()
@@ -385,8 +388,19 @@ def e2e_measure(w, dev, cu_np, steps, warmup):
     torch.cuda.synchronize()
     U.check()
     t = a.elapsed_time(b) / 1e3 / steps
+
+    # the host link on its own (one large pinned copy each way), which tells
+    # how much of the per-step traffic the compute can hide on this machine
+    def copy_gbs(dst, src):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(main)
+        dst.copy_(src, non_blocking=True)
+        e1.record(main)
+        torch.cuda.synchronize()
+        return src.numel() * src.element_size() / (e0.elapsed_time(e1) / 1e3) / 1e9
+    link = {"h2d_gbs": copy_gbs(bufs[0][0], hq), "d2h_gbs": copy_gbs(hdq, grads[0][0])}
     return {"value": w.B * w.S / t, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": t * 1e3}
+            "d2h_bytes_per_step": d2h, "ms_per_step": t * 1e3, "host_link": link}
 
 
 def ring_measure(w, dev, steps, warmup):
