@@ -422,8 +422,13 @@ int launch_fwd_dc(const AttnArgs& a, cudaStream_t st) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaLaunchKernelEx(&cfg, tc_fwd_kernel<D, CL>, tq, tk, tv, (__nv_bfloat16*)a.o_out, a.lse, a.S, a.nq, a.G,
-                     a.lse_bstride, a.cu, a.nd, a.causal, a.scale * kLog2e, a.seq, a.hq_tot);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, tc_fwd_kernel<D, CL>, tq, tk, tv, (__nv_bfloat16*)a.o_out, a.lse,
+                                           a.S, a.nq, a.G, a.lse_bstride, a.cu, a.nd, a.causal, a.scale * kLog2e,
+                                           a.seq, a.hq_tot);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();   // the error is reported here, not left for the next call
+    return set_error(ULYSSES_ERR_CUDA, "tc_fwd: cluster launch failed: %s", cudaGetErrorString(e));
+  }
   count_launch();
   return check_launch("tc_fwd");
 }
