@@ -621,7 +621,8 @@ def gpu_arm(args):
         "roofline": {"kernel": "attn_bwd", "bound": "tensor", "achieved": achieved,
                      "peak": bf16, "unit": "TFLOP/s", "frac": achieved / bf16,
                      "traffic": measured_traffic(w.name),
-                     "peak_source": f"{peak_src} bf16 dense (burst)"},
+                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "frac_of_sustained_peak": achieved / bf16_sus if bf16_sus else None},
         "gpu_launches": launches,
         "clocks": clk,
         "e2e": e2e,
