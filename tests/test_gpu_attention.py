@@ -59,6 +59,12 @@ SMALL = [
     # many key blocks of unequal work: the backward's decreasing-work block order
     (3000, 4, 2, 128, 1, 4, "bf16", [700, 5, 123, 1000, 128, 256, 300, 488], True),
     (2100, 4, 2, 128, 1, 4, "bf16", [128, 512, 640, 64, 756], False),
+    # G = 8 (the forward's pairs take two of the eight q heads of a kv head)
+    (2048, 8, 1, 128, 1, 8, "bf16", None, True),
+    # D = 64 at a length where the tensor-core forward runs over many key tiles
+    (1536, 4, 2, 64, 1, 4, "bf16", [700, 836], True),
+    # bidirectional documents over many tiles, two ranks
+    (4096, 4, 2, 128, 2, 2, "bf16", [1000, 3096], False),
 ]
 
 
