@@ -611,7 +611,7 @@ def gpu_arm(args):
         "frac_fwd_bwd_of_nominal_bf16": (fl_fwd + fl_bwd) / (t_fwd + t_bwd) / 1e12 / NOMINAL_BF16_TFLOPS,
         "peaks": {"bf16_tflops": bf16, "hbm_gbs": hbm, "source": peak_src,
                   "nominal_bf16_tflops": NOMINAL_BF16_TFLOPS, "nominal_hbm_gbs": NOMINAL_HBM_GBS,
-                  "targets_judged_against": "the measured peaks (frac_* keys without 'nominal')"},
+                  "targets_measured_against": "the measured peaks (frac_* keys without 'nominal')"},
         "relayout_gbs": relay_step_gbs, "relayout_frac_hbm": relay_step_gbs / hbm,
         "relayout_ms_per_step": t_relayout * 1e3,
         "relayout_bytes_per_step": relay_bytes,
