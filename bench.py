@@ -592,6 +592,10 @@ def gpu_arm(args):
     if not args.kernels_only:
         relay_gbs, _ = measure_relayout(w, dev)
         e2e = e2e_measure(w, dev, cu_np, max(1, args.steps), max(1, args.warmup // 2))
+        # whole job, like `value`: every replica's tokens over the slowest replica's time
+        e2e_t = reduce_max(e2e["ms_per_step"] / 1e3, dev)
+        e2e["ms_per_step"] = e2e_t * 1e3
+        e2e["value"] = job_tokens_per_s(world, w.B, w.S, e2e_t)
         ring = ring_measure(w, dev, max(1, args.steps // 2), 1) if args.ring else None
         proj = proj_measure(w, dev) if args.proj else None
         fused = fused_measure(w, dev, cu_np, max(1, args.steps // 2), 1) if args.fused else None
